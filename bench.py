@@ -1,0 +1,447 @@
+"""Benchmark of the product-VQ KV-cache hot path on GB300.
+
+Default workload (N=1): single-sequence decode -- encode 8192 new keys of
+B=1, H=8, D=128 (uint8 codes, 256x4 codebook) and attend one query per head
+over the 8192 coded keys (values pre-encoded outside the timed region).
+One step = vq_encode_keys + vq_decode_attend (+ its combine pass).
+
+Other workloads (--workload): gqa-decode, bulk-encode, chunked-prefill.
+
+Prints ONE JSON line (rank 0).  `value` is device-timed throughput with
+inputs resident in HBM; `e2e` repeats the step through the same C-ABI calls
+from pinned host buffers with the host<->device copies inside the timed
+region.  L2 is flushed (a 256 MiB write) before every timed step.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the
+same workload (the CPU baseline); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from product_vq_compressed_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------- metrics
+
+METRICS = {
+    "decode-1seq": ("decode tokens/s (encode 8192 keys + attend, B=1 H=8 D=128)",
+                    "tokens/s"),
+    "gqa-decode": ("decode tokens/s (B=32 Hq=32 Hkv=8 S_kv=32768)", "tokens/s"),
+    "bulk-encode": ("key-encode vectors/s ([4,32,8192,128] K+V encode)", "vectors/s"),
+    "chunked-prefill": ("prefill tokens/s (S_q=2048, window 4096)", "tokens/s"),
+}
+
+
+def units_per_step(name, spec):
+    if name == "bulk-encode":
+        return spec.B * spec.H_kv * spec.enc_len       # key vectors
+    return spec.B * spec.S_q                           # query tokens
+
+
+def algorithmic(name, spec):
+    """(dominant kernel, bound, work per launch, unit) -- the per-unit
+    figures are stated with the design notes."""
+    if name in ("decode-1seq", "bulk-encode"):
+        n_sub = spec.B * spec.H_kv * spec.enc_len * spec.n_k
+        flops = 2.0 * spec.k_d * spec.k_N * n_sub     # one multiply-add per dim and candidate
+        return "encode", "alu", flops, "TFLOP/s"
+    if name == "gqa-decode":
+        per_tok = spec.n_k * np.dtype(spec.k_code_dtype).itemsize + \
+            spec.n_v * np.dtype(spec.v_code_dtype).itemsize
+        byts = spec.B * spec.H_kv * spec.S_kv * per_tok + \
+            2 * spec.B * spec.H_q * spec.S_q * spec.D * 2
+        return "decode", "hbm", float(byts), "GB/s"
+    # chunked prefill: QK^T and PV over each query's visible keys
+    vis = min(spec.window, spec.S_kv) if spec.window else spec.S_kv
+    flops = 4.0 * spec.D * spec.S_q * vis * spec.H_q * spec.B
+    return "prefill", "tensor", flops, "TFLOP/s"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def peak_for(bound, peaks):
+    if bound == "hbm":
+        return peaks["hbm_gbs"], "GB/s"
+    if bound == "tensor":
+        # fp16 inputs with fp32 accumulation run at the bf16 dense rate
+        return peaks["bf16_tflops"], "TFLOP/s"
+    # fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock
+    return 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, "TFLOP/s"
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, r in rows for k in range(4)
+                          if r[k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+class Runner:
+    """Holds device inputs of one workload and runs one step."""
+
+    def __init__(self, name, spec, inp, torch, vq, stream):
+        self.name, self.spec, self.torch, self.vq = name, spec, torch, vq
+        self.stream = stream
+        t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        self.d = {k: t(v) for k, v in inp.items() if isinstance(v, np.ndarray)}
+        s = spec
+        dev = self.d
+        self.launches = 0
+        if name == "decode-1seq":
+            # values pre-encoded once, outside the timed region
+            dev["v_codes"], _ = vq.encode_values(dev["values"], dev["v_codebook"], s.v_d,
+                                                 stream=stream)
+            dev["k_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_k),
+                                         dtype=vq.code_dtype(s.k_N), device="cuda")
+        if name == "bulk-encode":
+            dev["k_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_k),
+                                         dtype=vq.code_dtype(s.k_N), device="cuda")
+            dev["v_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_v),
+                                         dtype=vq.code_dtype(s.v_N), device="cuda")
+            dev["k_hat"] = torch.empty_like(dev["keys"])
+        dev["out"] = torch.empty_like(dev["q"])
+        if name != "bulk-encode":
+            args = vq.make_attend_args(dev["q"], dev["k_codes"], dev["k_codebook"],
+                                       dev["v_codes"], dev["v_codebook"],
+                                       dev.get("smooth"), s.sm_scale, s.causal,
+                                       s.window, dev["out"])
+            need = vq.attend_workspace_bytes(args)
+            dev["ws"] = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+
+    def step(self, ev=None):
+        """One pass of the hot path; ev = (start, mid) events around the
+        dominant kernel (recorded on the launch stream)."""
+        s, d, vq, st = self.spec, self.d, self.vq, self.stream
+        if self.name == "decode-1seq":
+            if ev: ev[0].record(st)
+            vq.encode_keys(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
+                           codes=d["k_codes"], stream=st)
+            if ev: ev[1].record(st)
+            vq.decode_attend(d["q"], d["k_codes"], d["k_codebook"], d["v_codes"],
+                             d["v_codebook"], d["smooth"], s.sm_scale, s.causal,
+                             s.window, out=d["out"], workspace=d["ws"], stream=st)
+            return 3
+        if self.name == "bulk-encode":
+            if ev: ev[0].record(st)
+            vq.encode_keys(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
+                           codes=d["k_codes"], k_hat=d["k_hat"], stream=st)
+            if ev: ev[1].record(st)
+            vq.encode_values(d["values"], d["v_codebook"], s.v_d, codes=d["v_codes"],
+                             stream=st)
+            return 2
+        fn = vq.prefill_attend if self.name == "chunked-prefill" else vq.decode_attend
+        if ev: ev[0].record(st)
+        fn(d["q"], d["k_codes"], d["k_codebook"], d["v_codes"], d["v_codebook"],
+           d["smooth"], s.sm_scale, s.causal, s.window, out=d["out"],
+           workspace=d["ws"], stream=st)
+        if ev: ev[1].record(st)
+        return 2
+
+
+def run_gpu(args, name, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from product_vq_compressed_gb300 import binding as vq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    spec = WORKLOADS[name]
+    inp = make_inputs(spec)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        r = Runner(name, spec, inp, torch, vq, stream)
+    torch.cuda.synchronize()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    for _ in range(args.warmup):
+        r.step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    launches = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for k in range(K):
+            flush.fill_(float(k))            # evict L2 between timed steps
+            stream.wait_stream(torch.cuda.current_stream())
+            e_start, e_mid, e_end = evs[k]
+            launches += r.step(ev=(e_start, e_mid))
+            e_end.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    step_ms = [evs[k][0].elapsed_time(evs[k][2]) for k in range(K)]
+    dom_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(K)]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    units = units_per_step(name, spec) * K * world
+    value = units / total_s
+
+    # ---- end to end from pinned host buffers (same C-ABI calls)
+    e2e = None
+    if name in ("decode-1seq", "gqa-decode", "chunked-prefill", "bulk-encode"):
+        in_keys = ["keys", "q"] if name == "decode-1seq" else (
+            ["keys", "values"] if name == "bulk-encode" else ["q"])
+        host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+                for k in in_keys}
+        out_name = "k_codes" if name == "bulk-encode" else "out"
+        host_out = torch.empty(r.d[out_name].shape, dtype=r.d[out_name].dtype).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for h in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                for k in in_keys:
+                    r.d[k].copy_(host[k], non_blocking=True)
+                r.step()
+                host_out.copy_(r.d[out_name], non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        Ke = max(3, min(K, 20))
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(Ke):
+                for k in in_keys:
+                    r.d[k].copy_(host[k], non_blocking=True)
+                r.step()
+                host_out.copy_(r.d[out_name], non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        e2e = {"value": units_per_step(name, spec) * Ke / e2e_s,
+               "unit": METRICS[name][1], "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    kernel, bound, work, wunit = algorithmic(name, spec)
+    peaks, peak_src = load_peaks()
+    peak, punit = peak_for(bound, peaks)
+    dom_s = statistics.mean(dom_ms) / 1e3
+    achieved = (work / dom_s) / (1e9 if wunit == "GB/s" else 1e12)
+    roof = {"bound": bound, "kernel": kernel, "achieved": round(achieved, 3),
+            "peak": round(peak, 1), "unit": punit, "frac": round(achieved / peak, 4),
+            "peak_source": peak_src, "traffic": None,
+            "kernel_ms": round(dom_s * 1e3, 4)}
+    clocks = clk.summary()
+    metric, unit = METRICS[name]
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "B": spec.B, "H_q": spec.H_q, "H_kv": spec.H_kv,
+                   "D": spec.D, "S_kv": spec.S_kv, "S_q": spec.S_q,
+                   "k_codebook": [spec.k_N, spec.k_d], "v_codebook": [spec.v_N, spec.v_d],
+                   "sliding_window": spec.window, "l2": "flushed before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": e2e, "gpu_launches": launches, "roofline": roof, "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, spec, inp, budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------- CPU arm (oracle)
+
+def cpu_baseline(name, spec, inp, budget_s=15.0):
+    """Time the float64 oracle, as it stands, on a bounded sample of the
+    workload and scale it to the metric's unit (one thread)."""
+    import oracle
+    oracle.build()
+    D = spec.D
+    rng = np.random.default_rng(0)
+
+    def time_encode(n_vec):
+        keys = inp["keys"].reshape(-1, D)
+        heads = np.broadcast_to(np.arange(spec.H_kv)[None, :, None],
+                                inp["keys"].shape[:3]).reshape(-1)
+        idx = rng.integers(0, keys.shape[0], n_vec)
+        t0 = time.perf_counter()
+        oracle.encode(keys[idx], inp["k_codebook"], heads=heads[idx], smooth=inp["smooth"])
+        return time.perf_counter() - t0
+
+    def time_attend(n_rows):
+        """Oracle attention of n_rows rows of one (batch, kv head): the
+        K_hat reconstruction of that head plus the rows."""
+        if "k_codes" in inp:
+            kc, vc = inp["k_codes"][:1, :1], inp["v_codes"][:1, :1]
+        else:
+            kc = rng.integers(0, spec.k_N, (1, 1, spec.S_kv, spec.n_k))
+            vc = rng.integers(0, spec.v_N, (1, 1, spec.S_kv, spec.n_v))
+        rows = np.array([[0, r % spec.G, spec.S_q - 1 - (r // spec.G) % spec.S_q]
+                         for r in range(n_rows)])
+        t0 = time.perf_counter()
+        oracle.attend_rows(inp["q"][:1, :spec.G], kc, inp["k_codebook"], vc,
+                           inp["v_codebook"], None if inp["smooth"] is None else inp["smooth"][:1],
+                           spec.sm_scale, spec.causal, spec.window, rows)
+        return time.perf_counter() - t0
+
+    def attend_model():
+        t1, t5 = time_attend(1), time_attend(5)
+        per_row = max((t5 - t1) / 4, 0.0)
+        per_head = max(t1 - per_row, 0.0)
+        return per_head, per_row
+
+    n_bg = spec.B * spec.H_kv
+    n_rows = spec.B * spec.H_q * spec.S_q
+    if name in ("decode-1seq", "bulk-encode"):
+        n_total = spec.B * spec.H_kv * spec.enc_len
+        per = time_encode(64) / 64
+        n_s = int(max(64, min(n_total, 0.6 * budget_s / max(per, 1e-9))))
+        full = time_encode(n_s) * n_total / n_s
+        sample = f"oracle key encode of {n_s} of {n_total} vectors, scaled"
+        if name == "decode-1seq":
+            per_head, per_row = attend_model()
+            full += n_bg * per_head + n_rows * per_row
+            sample += (f"; oracle attention of 1 and 5 rows of one kv head over "
+                       f"{spec.S_kv} keys, scaled to {n_bg} heads and {n_rows} rows")
+            value = spec.B * spec.S_q / full
+        else:
+            value = n_total / full
+    else:
+        per_head, per_row = attend_model()
+        full = n_bg * per_head + n_rows * per_row
+        value = spec.B * spec.S_q / full
+        sample = (f"oracle attention of 1 and 5 rows of one (batch, kv head) over "
+                  f"{spec.S_kv} keys, scaled to {n_bg} pairs and {n_rows} rows")
+    return {"value": value, "unit": METRICS[name][1], "cores": 1, "kind": "oracle",
+            "sample": sample, "est_step_s": full}
+
+
+def run_reference(args, name):
+    spec = WORKLOADS[name]
+    inp = make_inputs(spec)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(name, spec, inp, budget_s=2.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(name, spec, inp, budget_s=args.cpu_budget / max(1, args.steps)))
+    wall = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    metric, unit = METRICS[name]
+    cb = dict(vals[-1])
+    cb["value"] = v
+    return {"impl": "reference", "metric": metric, "value": v, "unit": unit,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "B": spec.B, "H_q": spec.H_q, "H_kv": spec.H_kv,
+                       "D": spec.D, "S_kv": spec.S_kv, "S_q": spec.S_q},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode-1seq", choices=sorted(METRICS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, args.workload)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = run_gpu(args, args.workload, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

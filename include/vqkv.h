@@ -1,0 +1,210 @@
+/*
+ * vqkv.h -- C ABI of libvqkv.so, a product-vector-quantised KV cache for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow three documentation pages of a VecInfer-style cache:
+ *   "Metal Kernels API" (veloxquant.dev/docs/api/metal-api), sections
+ *     "VecInfer kernels" and "Fused SDPA";
+ *   "Metal GPU Kernels" guide (veloxquant.dev/docs/guides/metal-kernels),
+ *     section "Fused SDPA kernel";
+ *   "veloxquant_mlx.cache.vecinfer_cache module" (VecInferKVCache).
+ * Each entry point below names the passage that defines it.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are caller-owned, contiguous, row-major, and live in device
+ *     memory (or memory the device can address).  The library allocates
+ *     nothing and keeps no state between calls; scratch space, where an
+ *     operation needs it, is passed in by the caller.
+ *   - fp16 tensors are IEEE binary16 (passed as void*); codebooks, smooth
+ *     factors and fp32 outputs are IEEE binary32.
+ *   - Codes are unsigned integers of `code_bytes` bytes each: 1 (uint8,
+ *     n_centroids <= 256) or 2 (uint16, n_centroids <= 65536).
+ *   - Every pointer must be 16-byte aligned (vectorised 128-bit accesses).
+ *   - Checks run in this order: sizes (VQ_ERR_SHAPE), limits
+ *     (VQ_ERR_UNSUPPORTED), then -- unless the problem is empty, which
+ *     returns VQ_OK without reading any pointer -- pointers (VQ_ERR_NULL)
+ *     and alignment (VQ_ERR_ALIGN), then workspace size.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  All work is enqueued asynchronously on it; arguments are
+ *     validated on the host before anything is enqueued, so an error status
+ *     means nothing was launched (except VQ_ERR_CUDA, which reports a failed
+ *     launch).
+ *   - The library never aborts, exits or traps on the device.
+ */
+#ifndef VQKV_H_
+#define VQKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VQ_API __attribute__((visibility("default")))
+#else
+#define VQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VQ_OK = 0,
+    VQ_ERR_NULL = -1,        /* a required pointer is NULL                   */
+    VQ_ERR_SHAPE = -2,       /* inconsistent sizes (e.g. D % sub_dim != 0)   */
+    VQ_ERR_UNSUPPORTED = -3, /* valid request outside this build's limits    */
+    VQ_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned             */
+    VQ_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required   */
+    VQ_ERR_CUDA = -6         /* a CUDA launch or query failed                */
+} vq_status;
+
+/* Static, human-readable description of a status code (never NULL). */
+VQ_API const char *vq_status_str(int status);
+
+/*
+ * Key encode.  Page: "Metal Kernels API", section "VecInfer kernels",
+ * vecinfer_encode_decode_metal (smooth -> Walsh-Hadamard transform -> VQ
+ * encode -> dequant -> inverse-WHT -> inverse-smooth), with the search of
+ * vecinfer_quantize_metal; the module summary of
+ * "veloxquant_mlx.cache.vecinfer_cache" describes the same smooth + rotation.
+ *
+ *   keys_f16   [B, H, S, D] fp16.
+ *   codebook   [n_centroids, sub_dim] fp32, shared by all sub-vector
+ *              positions and heads.
+ *   smooth     smooth_mode 0: NULL (no smoothing); 1: [D]; 2: [H, D] fp32,
+ *              finite and non-zero.
+ *   codes      [B, H, S, D/sub_dim] of code_bytes each (output).
+ *   k_hat_f16  [B, H, S, D] fp16 reconstruction (output) or NULL to skip.
+ *
+ * Per vector x of head h: y = Hn (s_h (.) x) with Hn the normalised
+ * Sylvester-Hadamard matrix; code_m = the nearest centroid of sub-vector
+ * y[m*sub_dim : (m+1)*sub_dim] by squared Euclidean distance in fp32, the
+ * lowest index on ties; k_hat = s_h^-1 (.) Hn concat_m codebook[code_m],
+ * rounded to fp16 (nearest even).
+ *
+ * Errors: VQ_ERR_NULL (keys, codebook, codes, or smooth when smooth_mode
+ * != 0), VQ_ERR_SHAPE (a size < 0, D % sub_dim != 0, smooth_mode not in
+ * 0..2, code_bytes not 1 or 2), VQ_ERR_UNSUPPORTED (D not a power of two in
+ * [32, 512], sub_dim not in {1, 2, 4, 8, 16}, n_centroids < 1 or above the
+ * code width, or a codebook larger than 160 KiB), VQ_ERR_ALIGN, VQ_ERR_CUDA.
+ * B, H or S equal to 0 is a no-op (pointers may then be NULL).
+ */
+VQ_API int vq_encode_keys(const void *keys_f16, int B, int H, int S, int D,
+                   const float *codebook, int n_centroids, int sub_dim,
+                   const float *smooth, int smooth_mode, void *codes,
+                   int code_bytes, void *k_hat_f16, void *stream);
+
+/*
+ * Value encode.  Page: "Metal Kernels API", section "VecInfer kernels",
+ * vecinfer_encode_decode_simple_metal, the value-side sibling of the key
+ * encoder without the smooth and Hadamard steps.
+ *
+ * Same arguments, limits and errors as vq_encode_keys without smooth: per
+ * vector, code_m = nearest centroid of x[m*sub_dim : (m+1)*sub_dim] (fp32
+ * squared distance, lowest index on ties); v_hat (optional) =
+ * concat_m codebook[code_m] rounded to fp16.
+ */
+VQ_API int vq_encode_values(const void *values_f16, int B, int H, int S, int D,
+                     const float *codebook, int n_centroids, int sub_dim,
+                     void *codes, int code_bytes, void *v_hat_f16,
+                     void *stream);
+
+/*
+ * Codebook gather.  Page: "Metal Kernels API", section "VecInfer kernels",
+ * vecinfer_dequant_metal.
+ *
+ *   codes   [n_vectors, n_sub] of code_bytes each.
+ *   out     [n_vectors, n_sub * sub_dim]: fp32 when out_is_f32 != 0, else
+ *           fp16 (nearest even).
+ * out[v, m*sub_dim + t] = codebook[codes[v, m], t].  A code >= n_centroids
+ * is a caller error: its output row is undefined, but every memory access
+ * stays in bounds (the code is clamped).
+ * Errors: VQ_ERR_NULL, VQ_ERR_SHAPE (negative sizes, n_sub or sub_dim < 1,
+ * code_bytes not 1 or 2), VQ_ERR_UNSUPPORTED (n_centroids above the code
+ * width), VQ_ERR_ALIGN, VQ_ERR_CUDA.  n_vectors == 0 is a no-op.
+ */
+VQ_API int vq_dequant(const void *codes, int code_bytes, int64_t n_vectors, int n_sub,
+               const float *codebook, int n_centroids, int sub_dim, void *out,
+               int out_is_f32, void *stream);
+
+/*
+ * Arguments of attention over the coded cache.  Page: "Metal Kernels API",
+ * section "Fused SDPA", metal_fused_sdpa, with the query semantics of
+ * VecInferKVCache.fused_sdpa ("veloxquant_mlx.cache.vecinfer_cache module"):
+ * the caller passes the raw query; the library applies the dual transform
+ * q~ = Hn (q (.) s_g^-1) itself, so that q~ . K~^T equals q . K_hat^T.
+ *
+ *   q_f16      [B, H_q, S_q, D] fp16, untransformed.
+ *   k_codes    [B, H_kv, S_kv, D/k_sub_dim] key codes (k_code_bytes each),
+ *              produced by vq_encode_keys with k_codebook and smooth.
+ *   v_codes    [B, H_kv, S_kv, D/v_sub_dim] value codes.
+ *   smooth     key smooth factors, as in vq_encode_keys.
+ *   scale      softmax scale (typically 1/sqrt(D)).
+ *   causal     != 0: queries align to the tail of the cache, row i sits at
+ *              q_abs = S_kv - S_q + i and sees keys j <= q_abs.
+ *   sliding_window  > 0: row i sees only keys j > q_abs - sliding_window
+ *              (the window ends at, and includes, the query's position).
+ *   out_f16    [B, H_q, S_q, D] fp16 (output).
+ *   workspace  device scratch of at least vq_attend_workspace_bytes(args)
+ *              bytes, 16-byte aligned; may be NULL when that size is 0.
+ * Query head h reads KV head h / (H_q / H_kv).  Softmax accumulates in fp32.
+ * The key and value codebooks are independent (sizes may differ).
+ */
+typedef struct {
+    int B, H_q, H_kv, S_q, S_kv, D;
+    const void *q_f16;
+    const void *k_codes;
+    int k_code_bytes;
+    const float *k_codebook;
+    int k_n_centroids, k_sub_dim;
+    const void *v_codes;
+    int v_code_bytes;
+    const float *v_codebook;
+    int v_n_centroids, v_sub_dim;
+    const float *smooth;
+    int smooth_mode;
+    float scale;
+    int causal;
+    int sliding_window;
+    void *out_f16;
+    void *workspace;
+    size_t workspace_bytes;
+} vq_attend_args;
+
+/*
+ * Scratch bytes vq_decode_attend / vq_prefill_attend need for `args` on the
+ * current device (split-KV partial results; 0 if none).  Depends only on the
+ * sizes in args and on the device's SM count.  Returns 0 for a NULL args.
+ */
+VQ_API size_t vq_attend_workspace_bytes(const vq_attend_args *args);
+
+/*
+ * Attention over the coded cache on CUDA cores + warp-level MMA, split
+ * across the key axis with a combine pass (flash-decoding).  Any S_q.
+ * Page: "Metal Kernels API", section "Fused SDPA", metal_fused_sdpa.
+ *
+ * Errors: VQ_ERR_NULL, VQ_ERR_SHAPE (negative sizes, H_kv == 0 or
+ * H_q % H_kv != 0, D % sub_dim != 0, S_q > S_kv when causal or windowed,
+ * S_kv == 0 with S_q > 0, negative window, bad smooth_mode or code width),
+ * VQ_ERR_UNSUPPORTED (D not a power of two in [32, 256], sub_dim not in
+ * {2, 4, 8}, codebooks over the on-chip limit, n_centroids above the code
+ * width), VQ_ERR_ALIGN, VQ_ERR_WORKSPACE, VQ_ERR_CUDA.
+ */
+VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
+
+/*
+ * Same operation through the tcgen05 tensor-core path (key/value tiles
+ * rebuilt from codes in shared memory, Q~K~^T and PV on the tensor cores,
+ * accumulators in tensor memory).  Used when S_q >= 64; smaller S_q, or
+ * shapes outside the tensor-core kernel's limits (D != 128, sub_dim != 4),
+ * are served by vq_decode_attend with the same arguments.  Page: "Metal
+ * Kernels API", section "Fused SDPA", metal_fused_sdpa; the prefill-shaped
+ * tile loop follows the companion described under rabitq_prefill_attend.
+ * Errors as vq_decode_attend.
+ */
+VQ_API int vq_prefill_attend(const vq_attend_args *args, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQKV_H_ */

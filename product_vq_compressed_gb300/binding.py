@@ -1,0 +1,251 @@
+"""Thin Python binding of libvqkv.so (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  The
+function names mirror the C entry points declared in include/vqkv.h.
+
+If the shared library has not been built, importing works but every call
+raises ``VQError`` naming the missing file; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+VQ_OK = 0
+VQ_ERR_NULL = -1
+VQ_ERR_SHAPE = -2
+VQ_ERR_UNSUPPORTED = -3
+VQ_ERR_ALIGN = -4
+VQ_ERR_WORKSPACE = -5
+VQ_ERR_CUDA = -6
+
+EXPORTED = ("vq_status_str", "vq_encode_keys", "vq_encode_values",
+            "vq_dequant", "vq_attend_workspace_bytes", "vq_decode_attend",
+            "vq_prefill_attend")
+
+
+class VQError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class AttendArgs(ctypes.Structure):
+    """Mirror of vq_attend_args."""
+
+    _fields_ = [
+        ("B", ctypes.c_int), ("H_q", ctypes.c_int), ("H_kv", ctypes.c_int),
+        ("S_q", ctypes.c_int), ("S_kv", ctypes.c_int), ("D", ctypes.c_int),
+        ("q_f16", ctypes.c_void_p),
+        ("k_codes", ctypes.c_void_p), ("k_code_bytes", ctypes.c_int),
+        ("k_codebook", ctypes.c_void_p),
+        ("k_n_centroids", ctypes.c_int), ("k_sub_dim", ctypes.c_int),
+        ("v_codes", ctypes.c_void_p), ("v_code_bytes", ctypes.c_int),
+        ("v_codebook", ctypes.c_void_p),
+        ("v_n_centroids", ctypes.c_int), ("v_sub_dim", ctypes.c_int),
+        ("smooth", ctypes.c_void_p), ("smooth_mode", ctypes.c_int),
+        ("scale", ctypes.c_float), ("causal", ctypes.c_int),
+        ("sliding_window", ctypes.c_int),
+        ("out_f16", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded ctypes library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise VQError(VQ_ERR_CUDA,
+                          f"libvqkv.so not built ({path}); run "
+                          "product_vq_compressed_gb300.build.build_library()")
+        L = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.vq_status_str.argtypes = [i32]
+        L.vq_status_str.restype = ctypes.c_char_p
+        L.vq_encode_keys.argtypes = [vp, i32, i32, i32, i32, vp, i32, i32, vp,
+                                     i32, vp, i32, vp, vp]
+        L.vq_encode_values.argtypes = [vp, i32, i32, i32, i32, vp, i32, i32,
+                                       vp, i32, vp, vp]
+        L.vq_dequant.argtypes = [vp, i32, i64, i32, vp, i32, i32, vp, i32, vp]
+        L.vq_attend_workspace_bytes.argtypes = [ctypes.POINTER(AttendArgs)]
+        L.vq_attend_workspace_bytes.restype = ctypes.c_size_t
+        L.vq_decode_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
+        L.vq_prefill_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
+        for fn in ("vq_encode_keys", "vq_encode_values", "vq_dequant",
+                   "vq_decode_attend", "vq_prefill_attend"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != VQ_OK:
+        raise VQError(status, f"{what}: {lib().vq_status_str(status).decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def code_dtype(n_centroids: int) -> torch.dtype:
+    return torch.uint8 if n_centroids <= 256 else torch.uint16
+
+
+def _code_bytes(t: torch.Tensor) -> int:
+    return t.element_size()
+
+
+def _smooth_mode(smooth: Optional[torch.Tensor]) -> int:
+    if smooth is None:
+        return 0
+    return 1 if smooth.dim() == 1 else 2
+
+
+def encode_keys(keys: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
+                smooth: Optional[torch.Tensor] = None,
+                codes: Optional[torch.Tensor] = None,
+                k_hat: Optional[torch.Tensor] = None, want_k_hat: bool = False,
+                stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """vq_encode_keys on keys [B, H, S, D] fp16; returns (codes, k_hat)."""
+    B, H, S, D = keys.shape
+    N = codebook.shape[0]
+    if codes is None:
+        codes = torch.empty((B, H, S, D // sub_dim), dtype=code_dtype(N),
+                            device=keys.device)
+    if k_hat is None and want_k_hat:
+        k_hat = torch.empty_like(keys)
+    st = lib().vq_encode_keys(_ptr(keys), B, H, S, D, _ptr(codebook), N,
+                              sub_dim, _ptr(smooth), _smooth_mode(smooth),
+                              _ptr(codes), _code_bytes(codes), _ptr(k_hat),
+                              _stream(stream))
+    _check(st, "vq_encode_keys")
+    return codes, k_hat
+
+
+def encode_values(values: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
+                  codes: Optional[torch.Tensor] = None,
+                  v_hat: Optional[torch.Tensor] = None,
+                  want_v_hat: bool = False, stream=None):
+    """vq_encode_values on values [B, H, S, D] fp16; returns (codes, v_hat)."""
+    B, H, S, D = values.shape
+    N = codebook.shape[0]
+    if codes is None:
+        codes = torch.empty((B, H, S, D // sub_dim), dtype=code_dtype(N),
+                            device=values.device)
+    if v_hat is None and want_v_hat:
+        v_hat = torch.empty_like(values)
+    st = lib().vq_encode_values(_ptr(values), B, H, S, D, _ptr(codebook), N,
+                                sub_dim, _ptr(codes), _code_bytes(codes),
+                                _ptr(v_hat), _stream(stream))
+    _check(st, "vq_encode_values")
+    return codes, v_hat
+
+
+def dequant(codes: torch.Tensor, codebook: torch.Tensor,
+            out: Optional[torch.Tensor] = None, out_f32: bool = True,
+            stream=None) -> torch.Tensor:
+    """vq_dequant: codes [..., n_sub] -> [..., n_sub * sub_dim]."""
+    N, d = codebook.shape
+    n_sub = codes.shape[-1]
+    n_vec = codes.numel() // n_sub if n_sub else 0
+    if out is None:
+        out = torch.empty(codes.shape[:-1] + (n_sub * d,),
+                          dtype=torch.float32 if out_f32 else torch.float16,
+                          device=codes.device)
+    st = lib().vq_dequant(_ptr(codes), _code_bytes(codes), n_vec, n_sub,
+                          _ptr(codebook), N, d, _ptr(out),
+                          int(out.dtype == torch.float32), _stream(stream))
+    _check(st, "vq_dequant")
+    return out
+
+
+def make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
+                     scale, causal=True, sliding_window=0, out=None,
+                     workspace=None) -> AttendArgs:
+    B, H_q, S_q, D = q.shape
+    _, H_kv, S_kv, _ = k_codes.shape
+    a = AttendArgs()
+    a.B, a.H_q, a.H_kv, a.S_q, a.S_kv, a.D = B, H_q, H_kv, S_q, S_kv, D
+    a.q_f16 = q.data_ptr()
+    a.k_codes = k_codes.data_ptr()
+    a.k_code_bytes = k_codes.element_size()
+    a.k_codebook = k_codebook.data_ptr()
+    a.k_n_centroids, a.k_sub_dim = k_codebook.shape
+    a.v_codes = v_codes.data_ptr()
+    a.v_code_bytes = v_codes.element_size()
+    a.v_codebook = v_codebook.data_ptr()
+    a.v_n_centroids, a.v_sub_dim = v_codebook.shape
+    a.smooth = 0 if smooth is None else smooth.data_ptr()
+    a.smooth_mode = _smooth_mode(smooth)
+    a.scale = float(scale)
+    a.causal = int(bool(causal))
+    a.sliding_window = int(sliding_window)
+    a.out_f16 = 0 if out is None else out.data_ptr()
+    a.workspace = 0 if workspace is None else workspace.data_ptr()
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return a
+
+
+def attend_workspace_bytes(args: AttendArgs) -> int:
+    return int(lib().vq_attend_workspace_bytes(ctypes.byref(args)))
+
+
+def _attend(fn_name, q, k_codes, k_codebook, v_codes, v_codebook, smooth,
+            scale=None, causal=True, sliding_window=0, out=None,
+            workspace=None, stream=None):
+    D = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
+                         scale, causal, sliding_window, out, workspace)
+    if workspace is None:
+        need = attend_workspace_bytes(a)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            a.workspace = workspace.data_ptr()
+            a.workspace_bytes = need
+    st = getattr(lib(), fn_name)(ctypes.byref(a), _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def decode_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
+                  scale=None, causal=True, sliding_window=0, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    """vq_decode_attend; raw q [B, H_q, S_q, D] fp16 -> out (same shape)."""
+    return _attend("vq_decode_attend", q, k_codes, k_codebook, v_codes,
+                   v_codebook, smooth, scale, causal, sliding_window, out,
+                   workspace, stream)
+
+
+def prefill_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
+                   scale=None, causal=True, sliding_window=0, out=None,
+                   workspace=None, stream=None) -> torch.Tensor:
+    """vq_prefill_attend (tensor-core path for S_q >= 64)."""
+    return _attend("vq_prefill_attend", q, k_codes, k_codebook, v_codes,
+                   v_codebook, smooth, scale, causal, sliding_window, out,
+                   workspace, stream)

@@ -1,0 +1,280 @@
+// encode.cu -- key / value encode (smooth, Walsh-Hadamard rotation, nearest
+// centroid per sub-vector) and the codebook gather.
+//
+// Pages: "Metal Kernels API", section "VecInfer kernels":
+//   vecinfer_encode_decode_metal  smooth -> WHT -> VQ encode -> dequant ->
+//                                 inverse WHT -> inverse smooth (keys);
+//   vecinfer_encode_decode_simple_metal  the same without smooth and WHT
+//                                 (values);
+//   vecinfer_quantize_metal       squared distances to every centroid kept in
+//                                 registers, one index per sub-vector;
+//   vecinfer_dequant_metal        codebook gather.
+//
+// GB300 layout.  A block of 256 threads stages the whole codebook (fp32) in
+// shared memory once and then walks a persistent loop over tiles of 512
+// sub-vectors (512 / n_sub tokens):
+//   1. one warp per token: fp16 load (8-byte vectors, coalesced), smooth and
+//      1/sqrt(D) folded into the load, in-place FWHT in shared memory;
+//   2. every thread owns two sub-vectors and scans the codebook; all threads
+//      read the same centroid at the same time, so each shared-memory read
+//      is a broadcast, and one centroid load serves both sub-vectors;
+//      fp32 direct-form distances sum_t (y_t - c_t)^2, strict '<' keeps the
+//      lowest index on ties; codes are written in sub-vector order
+//      (coalesced uint8 / uint16 stores);
+//   3. optional reconstruction: the chosen centroids replace the sub-vectors
+//      in shared memory, one warp per token runs the FWHT again (Hn is
+//      symmetric and its own inverse), divides by the smooth factors and
+//      stores fp16 (round to nearest even).
+// The scan of phase 2 is the cost: N * sub_dim fused multiply-adds plus a
+// compare/select per candidate.
+#include <math.h>
+
+#include "vq_internal.cuh"
+
+namespace vqkv {
+namespace {
+
+constexpr int kEncThreads = 256;
+constexpr int kSlots = 512;  // sub-vectors per tile (two per thread)
+
+// Unnormalised in-place Walsh-Hadamard transform (natural order) of the D
+// floats at v, by one warp.  Butterfly at stride h pairs i and i + h.
+__device__ __forceinline__ void warp_fwht(float *v, int D, int lane) {
+    for (int h = 1; h < D; h <<= 1) {
+        for (int p = lane; p < (D >> 1); p += 32) {
+            const int i = ((p & ~(h - 1)) << 1) | (p & (h - 1));
+            const float a = v[i], b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+        __syncwarp();
+    }
+}
+
+template <int SUBD>
+__device__ __forceinline__ void load_sub(const float *src, float (&dst)[SUBD]) {
+    if constexpr (SUBD % 4 == 0) {
+#pragma unroll
+        for (int t = 0; t < SUBD; t += 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(src + t);
+            dst[t] = q.x; dst[t + 1] = q.y; dst[t + 2] = q.z; dst[t + 3] = q.w;
+        }
+    } else if constexpr (SUBD == 2) {
+        const float2 q = *reinterpret_cast<const float2 *>(src);
+        dst[0] = q.x; dst[1] = q.y;
+    } else {
+        dst[0] = src[0];
+    }
+}
+
+template <int SUBD, typename CodeT>
+__global__ void __launch_bounds__(kEncThreads)
+encode_kernel(EncodeParams p, float inv_sqrt_d) {
+    extern __shared__ __align__(16) float smem[];
+    const int N = p.N, D = p.D;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *cb_s = smem;
+    float *y_s = smem + ((N * SUBD + 3) & ~3);
+
+    for (int i = tid; i < N * SUBD; i += kEncThreads) cb_s[i] = p.codebook[i];
+    __syncthreads();
+
+    const int n_sub = D / SUBD;
+    const int tok = kSlots / n_sub;  // tokens per tile (n_sub divides 512)
+    const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
+    CodeT *codes = reinterpret_cast<CodeT *>(p.codes);
+
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t v0 = tile * tok;
+        // ---- 1. load, smooth, rotate
+        for (int t = warp; t < tok; t += kEncThreads / 32) {
+            const int64_t v = v0 + t;
+            float *yv = y_s + t * D;
+            if (v < p.n_vec) {
+                const __half *xv = p.x + v * D;
+                const int h = (int)((v / p.S) % p.H);
+                const float *sm = p.smooth_mode == 2 ? p.smooth + (size_t)h * D
+                                                     : p.smooth;
+                for (int e = lane * 4; e < D; e += 128) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(xv + e);
+                    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+                    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                    float4 f = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    if (p.rotate) {
+                        if (p.smooth_mode != 0) {
+                            const float4 s = *reinterpret_cast<const float4 *>(sm + e);
+                            f.x *= s.x; f.y *= s.y; f.z *= s.z; f.w *= s.w;
+                        }
+                        f.x *= inv_sqrt_d; f.y *= inv_sqrt_d;
+                        f.z *= inv_sqrt_d; f.w *= inv_sqrt_d;
+                    }
+                    *reinterpret_cast<float4 *>(yv + e) = f;
+                }
+                __syncwarp();
+                if (p.rotate) warp_fwht(yv, D, lane);
+            } else {
+                for (int e = lane; e < D; e += 32) yv[e] = 0.f;
+            }
+        }
+        __syncthreads();
+
+        // ---- 2. nearest centroid of two sub-vectors per thread
+        {
+            const int s0 = tid, s1 = tid + kEncThreads;
+            float y0[SUBD], y1[SUBD];
+            load_sub<SUBD>(y_s + s0 * SUBD, y0);
+            load_sub<SUBD>(y_s + s1 * SUBD, y1);
+            float best0 = INFINITY, best1 = INFINITY;
+            int bi0 = 0, bi1 = 0;
+#pragma unroll 4
+            for (int c = 0; c < N; ++c) {
+                float cv[SUBD];
+                load_sub<SUBD>(cb_s + c * SUBD, cv);
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t) {
+                    const float e0 = y0[t] - cv[t];
+                    const float e1 = y1[t] - cv[t];
+                    d0 = fmaf(e0, e0, d0);
+                    d1 = fmaf(e1, e1, d1);
+                }
+                if (d0 < best0) { best0 = d0; bi0 = c; }
+                if (d1 < best1) { best1 = d1; bi1 = c; }
+            }
+            const int64_t g0 = v0 * n_sub + s0, g1 = v0 * n_sub + s1;
+            const int64_t lim = p.n_vec * n_sub;
+            if (g0 < lim) codes[g0] = (CodeT)bi0;
+            if (g1 < lim) codes[g1] = (CodeT)bi1;
+            if (p.xhat) {
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t) {
+                    y_s[s0 * SUBD + t] = cb_s[bi0 * SUBD + t];
+                    y_s[s1 * SUBD + t] = cb_s[bi1 * SUBD + t];
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- 3. optional reconstruction s^-1 (.) Hn y_hat -> fp16
+        if (p.xhat) {
+            for (int t = warp; t < tok; t += kEncThreads / 32) {
+                const int64_t v = v0 + t;
+                if (v >= p.n_vec) continue;
+                float *yv = y_s + t * D;
+                if (p.rotate) warp_fwht(yv, D, lane);
+                const int h = (int)((v / p.S) % p.H);
+                const float *sm = p.smooth_mode == 2 ? p.smooth + (size_t)h * D
+                                                     : p.smooth;
+                __half *ov = p.xhat + v * D;
+                for (int e = lane * 4; e < D; e += 128) {
+                    float4 f = *reinterpret_cast<const float4 *>(yv + e);
+                    if (p.rotate) {
+                        f.x *= inv_sqrt_d; f.y *= inv_sqrt_d;
+                        f.z *= inv_sqrt_d; f.w *= inv_sqrt_d;
+                        if (p.smooth_mode != 0) {
+                            const float4 s = *reinterpret_cast<const float4 *>(sm + e);
+                            f.x /= s.x; f.y /= s.y; f.z /= s.z; f.w /= s.w;
+                        }
+                    }
+                    __half2 lo = __floats2half2_rn(f.x, f.y);
+                    __half2 hi = __floats2half2_rn(f.z, f.w);
+                    uint2 raw;
+                    raw.x = *reinterpret_cast<uint32_t *>(&lo);
+                    raw.y = *reinterpret_cast<uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(ov + e) = raw;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <typename CodeT>
+__global__ void dequant_kernel(DequantParams p) {
+    const CodeT *codes = reinterpret_cast<const CodeT *>(p.codes);
+    const int64_t total = p.n_vec * p.n_sub;
+    const int d = p.sub_dim;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int c = (int)codes[i];
+        c = c < p.N ? c : p.N - 1;
+        const float *src = p.codebook + (size_t)c * d;
+        if (p.out_is_f32) {
+            float *dst = reinterpret_cast<float *>(p.out) + i * d;
+            for (int t = 0; t < d; ++t) dst[t] = src[t];
+        } else {
+            __half *dst = reinterpret_cast<__half *>(p.out) + i * d;
+            for (int t = 0; t < d; ++t) dst[t] = __float2half_rn(src[t]);
+        }
+    }
+}
+
+template <int SUBD, typename CodeT>
+cudaError_t launch_encode_t(const EncodeParams &p, cudaStream_t stream) {
+    const size_t smem = encode_smem_bytes(p.N, SUBD);
+    auto kern = encode_kernel<SUBD, CodeT>;
+    cudaError_t err = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount,
+                                      dev)) != cudaSuccess)
+        return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+             &per_sm, kern, kEncThreads, smem)) != cudaSuccess)
+        return err;
+    if (per_sm < 1) per_sm = 1;
+    const int n_sub = p.D / SUBD;
+    const int64_t tok = kSlots / n_sub;
+    const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > n_tiles) grid = n_tiles;
+    const float inv_sqrt_d = (float)(1.0 / sqrt((double)p.D));
+    kern<<<(unsigned)grid, kEncThreads, smem, stream>>>(p, inv_sqrt_d);
+    return cudaGetLastError();
+}
+
+template <int SUBD>
+cudaError_t launch_encode_c(const EncodeParams &p, cudaStream_t s) {
+    return p.code_bytes == 1 ? launch_encode_t<SUBD, uint8_t>(p, s)
+                             : launch_encode_t<SUBD, uint16_t>(p, s);
+}
+
+}  // namespace
+
+size_t encode_smem_bytes(int N, int sub_dim) {
+    return sizeof(float) * ((((size_t)N * sub_dim + 3) & ~(size_t)3) +
+                            (size_t)kSlots * sub_dim);
+}
+
+cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream) {
+    switch (p.sub_dim) {
+        case 1: return launch_encode_c<1>(p, stream);
+        case 2: return launch_encode_c<2>(p, stream);
+        case 4: return launch_encode_c<4>(p, stream);
+        case 8: return launch_encode_c<8>(p, stream);
+        case 16: return launch_encode_c<16>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaError_t err;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount,
+                                      dev)) != cudaSuccess)
+        return err;
+    const int threads = 256;
+    int64_t blocks = (p.n_vec * p.n_sub + threads - 1) / threads;
+    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+    if (blocks < 1) blocks = 1;
+    if (p.code_bytes == 1)
+        dequant_kernel<uint8_t><<<(unsigned)blocks, threads, 0, stream>>>(p);
+    else
+        dequant_kernel<uint16_t><<<(unsigned)blocks, threads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace vqkv
