@@ -203,6 +203,32 @@ VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
  */
 VQ_API int vq_prefill_attend(const vq_attend_args *args, void *stream);
 
+/*
+ * Allocation-free variant of vq_decode_attend.  The documentation pages have
+ * no counterpart: this is a service of this library for callers that cannot
+ * allocate device memory -- for example a plug-in inside a host application
+ * that owns all GPU memory, a runtime that fixes its memory plan before the
+ * model runs, or a latency-critical decode loop that must not call
+ * cudaMalloc (which can synchronise the device).
+ *
+ * Same arguments, results and errors as vq_decode_attend, except that
+ * args->workspace and args->workspace_bytes are ignored: the split-KV
+ * partial results go to a scratch array of VQ_NOALLOC_SCRATCH_BYTES compiled
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.  The library allocates nothing, here or anywhere.
+ *   - A problem whose partial results do not fit the array even with a
+ *     single key split returns VQ_ERR_WORKSPACE (larger problems otherwise
+ *     run with fewer splits); use vq_decode_attend with a workspace for those.
+ *   - All calls share the array: calls whose work overlaps on the GPU (other
+ *     streams or host threads) race on it; order them on one stream or with
+ *     events.  Every call overwrites what it reads, so no clearing is needed.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture.
+ */
+#define VQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+VQ_API int vq_decode_attend_noalloc(const vq_attend_args *args, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

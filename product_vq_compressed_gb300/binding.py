@@ -28,7 +28,7 @@ VQ_ERR_CUDA = -6
 
 EXPORTED = ("vq_status_str", "vq_encode_keys", "vq_encode_values",
             "vq_dequant", "vq_attend_workspace_bytes", "vq_decode_attend",
-            "vq_prefill_attend")
+            "vq_prefill_attend", "vq_decode_attend_noalloc")
 
 
 class VQError(RuntimeError):
@@ -87,8 +87,10 @@ def lib():
         L.vq_attend_workspace_bytes.restype = ctypes.c_size_t
         L.vq_decode_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
         L.vq_prefill_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
+        L.vq_decode_attend_noalloc.argtypes = [ctypes.POINTER(AttendArgs), vp]
         for fn in ("vq_encode_keys", "vq_encode_values", "vq_dequant",
-                   "vq_decode_attend", "vq_prefill_attend"):
+                   "vq_decode_attend", "vq_prefill_attend",
+                   "vq_decode_attend_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib

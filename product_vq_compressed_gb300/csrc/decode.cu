@@ -645,6 +645,27 @@ AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
     return p;
 }
 
+AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,
+                              size_t max_ws_bytes) {
+    AttendPlan p = plan_decode(a, num_sms);
+    if (p.ws_bytes <= max_ws_bytes) return p;
+    // fewer key splits until the partial results fit the given capacity
+    const int64_t units = (int64_t)a.B * a.H_kv * p.n_colblk;
+    const size_t per_split = (size_t)units * kCols * (a.D + 4) * sizeof(float);
+    const int64_t tiles = (a.S_kv + kTile - 1) / kTile;
+    const int64_t fit = per_split ? (int64_t)(max_ws_bytes / per_split) : 0;
+    if (fit < 1) {
+        p.n_split = 0;
+        p.ws_bytes = per_split;   // what one split alone would need
+        return p;
+    }
+    const int n = (int)(fit < p.n_split ? fit : p.n_split);
+    p.n_split = n;
+    p.tok_per_split = (int)(((tiles + n - 1) / n) * kTile);
+    p.ws_bytes = per_split * (size_t)n;
+    return p;
+}
+
 cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
                           cudaStream_t stream) {
     int dev = 0, sms = 0;

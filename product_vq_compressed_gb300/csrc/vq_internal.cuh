@@ -50,6 +50,10 @@ struct AttendPlan {
     size_t ws_bytes;    // partial results
 };
 AttendPlan plan_decode(const vq_attend_args &a, int num_sms);
+// The same plan with at most max_ws_bytes of partial results (fewer key
+// splits); n_split == 0 when even one split does not fit.
+AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,
+                              size_t max_ws_bytes);
 cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
                           cudaStream_t stream);
 size_t decode_smem_bytes(const vq_attend_args &a);
