@@ -38,12 +38,12 @@
 namespace vqkv {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kCols = 8;        // columns per item (MMA N)
-constexpr int kTile = 16;       // keys per MMA tile
-constexpr int kStepTiles = 2;   // tiles per softmax step
-constexpr int kStep = kTile * kStepTiles;
+// Warps of the one CTA per SM: 12 (up to 168 registers each) for D <= 128,
+// 8 for D = 256, whose accumulators need more registers per thread.
+__host__ __device__ constexpr int warps_for(int D) { return D >= 256 ? 8 : 12; }
+constexpr int kCols = 8;         // query columns per unit (MMA N)
+constexpr int kTile = 16;        // keys per MMA tile
+constexpr int kPrefetchTiles = 8;  // L2 prefetch distance
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ primitives
@@ -149,6 +149,34 @@ __device__ __forceinline__ void gather(uint32_t addr, uint32_t *w) {
     }
 }
 
+// Fast-path gathers: uint8 codes and one interleaved table of 256 rows x 256
+// bytes at shared-memory offset 0 -- row c holds the key centroid c replicas
+// in bytes [0, 128) and the value centroid c replicas in [128, 256).  The
+// address of the row for code byte i of word w plus the lane's replica
+// offset (< 256) is then a single byte permute: bytes (off, code, 0, 0).
+// i is a constant once the caller's loop is unrolled.
+__device__ __forceinline__ uint32_t row_off(uint32_t w, int i, uint32_t lane_off) {
+    return __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i << 4));
+}
+
+template <int SUB>
+__device__ __forceinline__ void gather_at(const unsigned char *p, uint32_t *w) {
+    if constexpr (SUB == 2) {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else if constexpr (SUB == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+}
+
+constexpr uint32_t kFastRow = 256;                 // bytes per interleaved row
+constexpr uint32_t kFastTable = 256 * kFastRow;    // 64 KiB
+
+__host__ __device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
 // ------------------------------------------------------------- the kernel
 
 struct DecArgs {
@@ -167,76 +195,312 @@ struct DecArgs {
     float sl;          // scale * log2(e)
     float inv_sqrt_d;
     int causal, window;
-    float *ws;         // partials [item][kCols][D + 4]
-    int n_split, n_colblk, tiles_per_split;
-    int64_t n_items;
-    int k_copies, v_copies;   // replicas per codebook row
+    float *ws;         // partial records [nw][slots][kCols][D + 4]
+    int n_colblk;
+    int tlo, T;        // every unit scans key tiles [tlo, tlo + T)
+    int64_t total;     // units * T, the flattened work
+    int nw;            // warps sharing the work
+    int slots;         // partial records per warp
+    int k_copies, v_copies;
 };
+
+// Start of warp gw's contiguous share of the flattened (unit, tile) space.
+__host__ __device__ __forceinline__ int64_t share_start(int64_t gw, int64_t total,
+                                                         int64_t nw) {
+    return gw * total / nw;
+}
 
 template <int D>
-struct Smem {
-    // codebook tables follow this struct in dynamic shared memory
-    float qt[kCols][D];                 // transformed queries (fp32)
-    float o[kWarps][kCols][D];          // per-warp partial outputs
-    float m[kWarps][kCols];
-    float l[kWarps][kCols];
-    int lo[kCols], hi[kCols];           // visible key range per column
+struct WarpScratch {
+    float work[D];            // fp32 FWHT buffer for one query column
+    __half qt[kCols][D];      // transformed queries (fp16 MMA operands)
+    int lo[kCols], hi[kCols]; // visible key range per column
 };
 
-template <int D, int DK, int DV>
-__global__ void __launch_bounds__(kThreads)
-decode_kernel(DecArgs a) {
-    constexpr int KSTEPS = D / 16;      // k-steps of the QK MMA
-    constexpr int MT = D / 16;          // M tiles of the PV MMA
-    constexpr int NKL = D / (4 * DK);   // key codes per lane and key
-    constexpr int NVL = D / (8 * DV);   // value codes per lane and key
-    constexpr int EK = 2 * DK, EV = 2 * DV;
-    constexpr int KW = (NKL * 2 + 3) / 4;   // words for NKL codes (<= 2 bytes)
-    constexpr int VW = (NVL * 2 + 3) / 4;
+constexpr int kStepTiles = 2;                 // tiles per softmax step
+constexpr int kStepKeys = kTile * kStepTiles;  // 32 keys
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
-    unsigned char *ktab = smem_raw + sizeof(Smem<D>);
-    const int krow = a.k_copies * EK;               // bytes per centroid row
-    unsigned char *vtab = ktab + (size_t)a.Nk * krow;
-    const int vrow = a.v_copies * EV;
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Codes of one step held in registers: for tile t, key rows g8 and g8 + 8
+// (K side) and keys 2c4, 2c4+1, 2c4+8, 2c4+9 (V side), each the lane's
+// contiguous run of sub-vector codes.
+template <int D, int DK, int DV>
+struct StepCodes {
+    static constexpr int NKL = D / (4 * DK);
+    static constexpr int NVL = D / (8 * DV);
+    static constexpr int KW = (NKL * 2 + 3) / 4;
+    static constexpr int VW = (NVL * 2 + 3) / 4;
+    uint32_t k[kStepTiles][2][KW];
+    uint32_t v[kStepTiles][4][VW];
+};
+
+// Row offsets (in keys) of the lane's K and V code rows inside a tile.
+__device__ __forceinline__ int krow_of(int g8, int r) { return g8 + 8 * r; }
+__device__ __forceinline__ int vrow_of(int c4, int r) { return 2 * c4 + (r & 1) + 8 * (r >> 1); }
+
+template <int D, int DK, int DV>
+__device__ __forceinline__ void load_step(StepCodes<D, DK, DV> &sc, const uint8_t *kl,
+                                          const uint8_t *vl, int j0, const DecArgs &a,
+                                          int64_t ktb, int64_t vtb, int g8, int c4) {
+    using SC = StepCodes<D, DK, DV>;
+    if (j0 + kStepKeys <= a.S_kv) {
+#pragma unroll
+        for (int t = 0; t < kStepTiles; ++t) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                load_codes<SC::NKL>(kl + (int64_t)(j0 + t * kTile + 8 * r) * ktb, a.kcb,
+                                    sc.k[t][r]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                load_codes<SC::NVL>(vl + (int64_t)(j0 + t * kTile + (r & 1) + 8 * (r >> 1)) * vtb,
+                                    a.vcb, sc.v[t][r]);
+        }
+    } else {  // tail of the cache: clamp rows past the last key (masked later)
+#pragma unroll
+        for (int t = 0; t < kStepTiles; ++t) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = min(j0 + t * kTile + krow_of(g8, r), a.S_kv - 1) - krow_of(g8, 0);
+                load_codes<SC::NKL>(kl + (int64_t)j * ktb, a.kcb, sc.k[t][r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int j = min(j0 + t * kTile + vrow_of(c4, r), a.S_kv - 1) - vrow_of(c4, 0);
+                load_codes<SC::NVL>(vl + (int64_t)j * vtb, a.vcb, sc.v[t][r]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void prefetch_l2(const uint8_t *p, uint32_t bytes) {
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (bytes & 15u) == 0 && bytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes)
+                     : "memory");
+}
+
+// Per-warp state of one unit (batch, kv head, column block).
+template <int D>
+struct UnitState {
+    uint32_t bq[D / 16][2];
+    float acc_o[D / 16][4];
+    float m0, m1, l0, l1;
+    int lo0, hi0, lo1, hi1;     // bounds of the lane's two columns
+    int lo_any, hi_any;         // keys every real column sees
+    int lo_all, hi_all;         // keys some column sees
+};
+
+// Gather of code u (a compile-time index after unrolling) of a code run.
+template <int DKV, int NC, bool FAST>
+__device__ __forceinline__ void gather_code(const uint32_t *words, int u, const DecArgs &a,
+                                            int cb, int N, uint32_t base, int row,
+                                            const unsigned char *tab, uint32_t lane_off,
+                                            uint32_t *w) {
+    if constexpr (FAST) {
+        gather_at<DKV>(tab + row_off(words[u >> 2], u & 3, lane_off), w);
+    } else {
+        const uint32_t code = min(code_at<NC>(words, cb, u), (uint32_t)(N - 1));
+        gather<DKV>(base + code * (uint32_t)row, w);
+    }
+}
+
+template <int D, int DK, int DV, bool FAST>
+__device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int j0,
+                                             UnitState<D> &u, const DecArgs &a,
+                                             uint32_t kbase, uint32_t vbase, int krow,
+                                             int vrow, int g8, int c4,
+                                             const unsigned char *tabs, uint32_t klane,
+                                             uint32_t vlane) {
+    using SC = StepCodes<D, DK, DV>;
+    constexpr int KSTEPS = D / 16, MT = D / 16;
+    if (j0 > u.hi_all || j0 + kStepKeys - 1 < u.lo_all) return;  // nobody sees it
+
+    // ---- S^T = K~ Q~^T for both tiles; even / odd k-steps accumulate
+    //      separately so the four MMA chains are independent
+    float s[kStepTiles][2][4];
+#pragma unroll
+    for (int t = 0; t < kStepTiles; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) s[t][h][0] = s[t][h][1] = s[t][h][2] = s[t][h][3] = 0.f;
+    uint32_t w8[kStepTiles][2][4];   // DK == 8: one gather serves two k-steps
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        uint32_t f[kStepTiles][2][2];
+#pragma unroll
+        for (int t = 0; t < kStepTiles; ++t) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if constexpr (DK == 4) {
+                    uint32_t w[2];
+                    gather_code<4, SC::NKL, FAST>(sc.k[t][r], ks, a, a.kcb, a.Nk, kbase, krow,
+                                                  tabs, klane, w);
+                    f[t][r][0] = w[0];
+                    f[t][r][1] = w[1];
+                } else if constexpr (DK == 2) {
+                    gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks, a, a.kcb, a.Nk, kbase,
+                                                  krow, tabs, klane, &f[t][r][0]);
+                    gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks + 1, a, a.kcb, a.Nk, kbase,
+                                                  krow, tabs, klane, &f[t][r][1]);
+                } else {
+                    if ((ks & 1) == 0)
+                        gather_code<8, SC::NKL, FAST>(sc.k[t][r], ks >> 1, a, a.kcb, a.Nk,
+                                                      kbase, krow, tabs, klane, w8[t][r]);
+                    f[t][r][0] = w8[t][r][2 * (ks & 1)];
+                    f[t][r][1] = w8[t][r][2 * (ks & 1) + 1];
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kStepTiles; ++t)
+            mma16816(s[t][ks & 1], f[t][0][0], f[t][1][0], f[t][0][1], f[t][1][1], u.bq[ks][0],
+                     u.bq[ks][1]);
+    }
+    // ---- scale, mask, online softmax for columns 2c4 and 2c4+1
+    float sc4[kStepTiles][4];
+    const bool need_mask = !(j0 >= u.lo_any && j0 + kStepKeys - 1 <= u.hi_any);
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < kStepTiles; ++t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float v = (s[t][0][e] + s[t][1][e]) * a.sl;
+            if (need_mask) {
+                const int j = j0 + t * kTile + g8 + 8 * (e >> 1);
+                const bool ok = (e & 1) ? (j >= u.lo1 && j <= u.hi1) : (j >= u.lo0 && j <= u.hi0);
+                v = ok ? v : -INFINITY;
+            }
+            sc4[t][e] = v;
+        }
+        mx0 = fmaxf(mx0, fmaxf(sc4[t][0], sc4[t][2]));
+        mx1 = fmaxf(mx1, fmaxf(sc4[t][1], sc4[t][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(u.m0, mx0), mn1 = fmaxf(u.m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    if (__any_sync(0xffffffffu, mn0 != u.m0 || mn1 != u.m1)) {
+        const float al0 = ex2(u.m0 - mu0), al1 = ex2(u.m1 - mu1);
+        u.l0 *= al0;
+        u.l1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            u.acc_o[mt][0] *= al0; u.acc_o[mt][2] *= al0;
+            u.acc_o[mt][1] *= al1; u.acc_o[mt][3] *= al1;
+        }
+    }
+    u.m0 = mn0;
+    u.m1 = mn1;
+    uint32_t bp[kStepTiles][2];
+#pragma unroll
+    for (int t = 0; t < kStepTiles; ++t) {
+        const float p0 = ex2(sc4[t][0] - mu0), p1 = ex2(sc4[t][1] - mu1);
+        const float p2 = ex2(sc4[t][2] - mu0), p3 = ex2(sc4[t][3] - mu1);
+        u.l0 += p0 + p2;
+        u.l1 += p1 + p3;
+        bp[t][0] = movmatrix_t(pack_h2(p0, p1));
+        bp[t][1] = movmatrix_t(pack_h2(p2, p3));
+    }
+    // ---- O^T += V_hat^T P^T, tile by tile
+    constexpr int WPL = D / 16;   // 32-bit value words per lane and key
+#pragma unroll
+    for (int t = 0; t < kStepTiles; ++t) {
+        uint32_t vw[4][WPL];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int uu = 0; uu < SC::NVL; ++uu)
+                gather_code<DV, SC::NVL, FAST>(sc.v[t][r], uu, a, a.vcb, a.Nv, vbase, vrow,
+                                               tabs, vlane, &vw[r][uu * (DV / 2)]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t a0 = __byte_perm(vw[0][mt], vw[1][mt], 0x5410);
+            const uint32_t a1 = __byte_perm(vw[0][mt], vw[1][mt], 0x7632);
+            const uint32_t a2 = __byte_perm(vw[2][mt], vw[3][mt], 0x5410);
+            const uint32_t a3 = __byte_perm(vw[2][mt], vw[3][mt], 0x7632);
+            mma16816(u.acc_o[mt], a0, a1, a2, a3, bp[t][0], bp[t][1]);
+        }
+    }
+}
+
+template <int D, int DK, int DV, bool FAST>
+__global__ void __launch_bounds__(warps_for(D) * 32, 1)
+decode_kernel(DecArgs a) {
+    constexpr int kWarps = warps_for(D), kThreads = kWarps * 32;
+    constexpr int KSTEPS = D / 16, MT = D / 16;
+    constexpr int EK = 2 * DK, EV = 2 * DV;
+    using SC = StepCodes<D, DK, DV>;
+
+    // shared memory: fp16 tables | per-warp scratch | fp32 staging
+    //   fast path: one interleaved 256 x 256-byte table (keys | values);
+    //   otherwise: key table (N_k rows) then value table (N_v rows)
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int krow = a.k_copies * EK, vrow = a.v_copies * EV;   // replica bytes per row
+    unsigned char *ktab = smem_raw;
+    unsigned char *vtab = FAST ? smem_raw + 128 : smem_raw + align16((size_t)a.Nk * krow);
+    const size_t tab_bytes = FAST ? (size_t)kFastTable
+                                  : align16((size_t)a.Nk * krow) + align16((size_t)a.Nv * vrow);
+    WarpScratch<D> *scratch = reinterpret_cast<WarpScratch<D> *>(smem_raw + tab_bytes);
+    float *stage = reinterpret_cast<float *>(scratch + kWarps);
+    const int kstride = FAST ? (int)kFastRow : krow;   // row strides of the tables
+    const int vstride = FAST ? (int)kFastRow : vrow;
+    const int nk_rows = FAST ? 256 : a.Nk, nv_rows = FAST ? 256 : a.Nv;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, c4 = lane & 3;
 
-    // ---- stage both codebooks as fp16, replicated per bank group
-    for (int i = tid; i < a.Nk * (krow / 4); i += kThreads) {
+    // ---- stage both codebooks: fp32 copy (coalesced), then fp16 tables
+    //      replicated per bank group (rows past N are zero on the fast path)
+    const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
+    for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
+    for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
+    __syncthreads();
+    for (int i = tid; i < nk_rows * (krow / 4); i += kThreads) {
         const int c = i / (krow / 4), wi = i % (krow / 4);
         const int t = ((wi * 4) % EK) / 2;
-        reinterpret_cast<uint32_t *>(ktab)[i] =
-            pack_h2(a.kcbk[c * DK + t], a.kcbk[c * DK + t + 1]);
+        *reinterpret_cast<uint32_t *>(ktab + (size_t)c * kstride + wi * 4) =
+            c < a.Nk ? pack_h2(stage[c * DK + t], stage[c * DK + t + 1]) : 0u;
     }
-    for (int i = tid; i < a.Nv * (vrow / 4); i += kThreads) {
+    for (int i = tid; i < nv_rows * (vrow / 4); i += kThreads) {
         const int c = i / (vrow / 4), wi = i % (vrow / 4);
         const int t = ((wi * 4) % EV) / 2;
-        reinterpret_cast<uint32_t *>(vtab)[i] =
-            pack_h2(a.vcbk[c * DV + t], a.vcbk[c * DV + t + 1]);
+        *reinterpret_cast<uint32_t *>(vtab + (size_t)c * vstride + wi * 4) =
+            c < a.Nv ? pack_h2(stage[nk_f + c * DV + t], stage[nk_f + c * DV + t + 1]) : 0u;
     }
-    const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(ktab) +
-                           (uint32_t)((lane % a.k_copies) * EK);
-    const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vtab) +
-                           (uint32_t)((lane % a.v_copies) * EV);
-    const int64_t k_tok_bytes = (int64_t)(D / DK) * a.kcb;
-    const int64_t v_tok_bytes = (int64_t)(D / DV) * a.vcb;
+    __syncthreads();
+    const uint32_t klane = (uint32_t)((lane % a.k_copies) * EK);
+    const uint32_t vlane = (FAST ? 128u : 0u) + (uint32_t)((lane % a.v_copies) * EV);
+    const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(ktab) + klane;
+    const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(smem_raw) + (FAST ? 0u : (uint32_t)(vtab - smem_raw)) + vlane;
+    const int64_t ktb = (int64_t)(D / DK) * a.kcb;   // code bytes per key
+    const int64_t vtb = (int64_t)(D / DV) * a.vcb;
     const int n_cols_total = a.G * a.S_q;
+    WarpScratch<D> &ws = scratch[warp];
 
-    for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-        const int split = (int)(item % a.n_split);
-        const int64_t rest = item / a.n_split;
-        const int cblk = (int)(rest % a.n_colblk);
-        const int64_t bg = rest / a.n_colblk;
-        const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    if (gw >= a.nw) return;
+    int64_t t = share_start(gw, a.total, a.nw);
+    const int64_t t_end = share_start(gw + 1, a.total, a.nw);
+    int slot = 0;
+    while (t < t_end) {
+        const int64_t unit = t / a.T;
+        const int64_t seg_end = min(t_end, (unit + 1) * (int64_t)a.T);
+        const int cblk = (int)(unit % a.n_colblk);
+        const int64_t bg = unit / a.n_colblk;
+        const int g = (int)(bg % a.H_kv);
+        const int b = (int)(bg / a.H_kv);
 
-        __syncthreads();  // previous item finished with the smem scratch
-        // ---- transformed queries: q~ = Hn (q (.) s_g^-1), one warp per column
-        for (int col = warp; col < kCols; col += kWarps) {
+        // ---- transformed queries of the unit's columns: q~ = Hn (q (.) s_g^-1)
+        __syncwarp();
+        for (int col = 0; col < kCols; ++col) {
             const int cg = cblk * kCols + col;
-            float *qv = sm.qt[col];
             if (cg < n_cols_total) {
                 const int i = cg / a.G, gam = cg % a.G;
                 const int hq = g * a.G + gam;
@@ -245,312 +509,204 @@ decode_kernel(DecArgs a) {
                 for (int e = lane; e < D; e += 32) {
                     float v = __half2float(qp[e]);
                     if (a.smooth_mode != 0) v = v / sp[e];
-                    qv[e] = v * a.inv_sqrt_d;
+                    ws.work[e] = v * a.inv_sqrt_d;
                 }
                 __syncwarp();
                 for (int h = 1; h < D; h <<= 1) {
                     for (int p = lane; p < D / 2; p += 32) {
                         const int x = ((p & ~(h - 1)) << 1) | (p & (h - 1));
-                        const float u = qv[x], w = qv[x + h];
-                        qv[x] = u + w;
-                        qv[x + h] = u - w;
+                        const float uu = ws.work[x], w = ws.work[x + h];
+                        ws.work[x] = uu + w;
+                        ws.work[x + h] = uu - w;
                     }
                     __syncwarp();
                 }
+                for (int e = lane; e < D; e += 32) ws.qt[col][e] = __float2half_rn(ws.work[e]);
                 if (lane == 0) {
                     const int q_abs = a.S_kv - a.S_q + i;
                     int hi = a.causal ? q_abs : a.S_kv - 1;
                     if (hi > a.S_kv - 1) hi = a.S_kv - 1;
                     int lo = a.window > 0 ? q_abs - a.window + 1 : 0;
                     if (lo < 0) lo = 0;
-                    sm.lo[col] = lo;
-                    sm.hi[col] = hi;
+                    ws.lo[col] = lo;
+                    ws.hi[col] = hi;
                 }
             } else {
-                for (int e = lane; e < D; e += 32) qv[e] = 0.f;
-                if (lane == 0) { sm.lo[col] = 1; sm.hi[col] = 0; }  // empty
+                for (int e = lane; e < D; e += 32) ws.qt[col][e] = __float2half_rn(0.f);
+                if (lane == 0) { ws.lo[col] = 1; ws.hi[col] = 0; }   // empty
             }
+            __syncwarp();
         }
-        __syncthreads();
-
-        // ---- query B fragments (fp16), dims permuted to match the gathers
-        uint32_t bq[KSTEPS][2];
+        UnitState<D> us;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
-            const float *qv = sm.qt[g8] + c4 * (D / 4) + 4 * ks;
-            bq[ks][0] = pack_h2(qv[0], qv[1]);
-            bq[ks][1] = pack_h2(qv[2], qv[3]);
+            const __half *qv = ws.qt[g8] + c4 * (D / 4) + 4 * ks;
+            us.bq[ks][0] = *reinterpret_cast<const uint32_t *>(qv);
+            us.bq[ks][1] = *reinterpret_cast<const uint32_t *>(qv + 2);
         }
-        // per-lane column bounds (lane owns columns 2*c4, 2*c4+1)
-        const int lo0 = sm.lo[2 * c4], hi0 = sm.hi[2 * c4];
-        const int lo1 = sm.lo[2 * c4 + 1], hi1 = sm.hi[2 * c4 + 1];
-        int lo_all = INT_MAX, hi_all = -1, lo_any = INT_MAX, hi_any = -1;
+        us.lo0 = ws.lo[2 * c4]; us.hi0 = ws.hi[2 * c4];
+        us.lo1 = ws.lo[2 * c4 + 1]; us.hi1 = ws.hi[2 * c4 + 1];
+        us.lo_all = INT_MAX; us.hi_all = -1; us.lo_any = 0; us.hi_any = INT_MAX;
         bool any_real = false;
 #pragma unroll
         for (int col = 0; col < kCols; ++col) {
-            const int l = sm.lo[col], h = sm.hi[col];
-            if (l > h) continue;     // padding / empty column
+            const int l = ws.lo[col], h = ws.hi[col];
+            if (l > h) continue;
             any_real = true;
-            lo_all = min(lo_all, l); hi_all = max(hi_all, h);   // union
-            lo_any = lo_any == INT_MAX ? l : max(lo_any, l);     // intersection
-            hi_any = hi_any == -1 ? h : min(hi_any, h);
+            us.lo_all = min(us.lo_all, l); us.hi_all = max(us.hi_all, h);
+            us.lo_any = max(us.lo_any, l); us.hi_any = min(us.hi_any, h);
         }
-        // this item's key range, clipped to what any column can see
-        const int t_begin = split * a.tiles_per_split * kTile;
-        int t_end = t_begin + a.tiles_per_split * kTile;
-        if (t_end > a.S_kv) t_end = a.S_kv;
-        const int r_begin = max(t_begin, any_real ? (lo_all & ~(kTile - 1)) : t_end);
-        const int r_end = min(t_end, any_real ? hi_all + 1 : t_begin);
-        // keys every real column sees inside [t_begin, t_end)
-        const int full_lo = max(t_begin, any_real ? lo_any : INT_MAX);
-        const int full_hi = min(t_end - 1, hi_any);
-        // per-lane bounds, restricted to this split
-        const int lo0s = max(lo0, t_begin), hi0s = min(hi0, t_end - 1);
-        const int lo1s = max(lo1, t_begin), hi1s = min(hi1, t_end - 1);
-
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float acc_o[MT][4];
+        if (!any_real) { us.lo_any = 1; us.hi_any = 0; }
+        us.m0 = us.m1 = -INFINITY;
+        us.l0 = us.l1 = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
-            acc_o[mt][0] = acc_o[mt][1] = acc_o[mt][2] = acc_o[mt][3] = 0.f;
+            us.acc_o[mt][0] = us.acc_o[mt][1] = us.acc_o[mt][2] = us.acc_o[mt][3] = 0.f;
 
-        const uint8_t *kbase_g = a.kc + (int64_t)bg * a.S_kv * k_tok_bytes;
-        const uint8_t *vbase_g = a.vc + (int64_t)bg * a.S_kv * v_tok_bytes;
+        const uint8_t *kg = a.kc + bg * a.S_kv * ktb;
+        const uint8_t *vg = a.vc + bg * a.S_kv * vtb;
+        // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
+        const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
+        const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
+        // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
+        const int j_first = (int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile);
+        const int j_last = (int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile);  // exclusive
+        auto prefetch = [&](int j) {
+            if (lane == 0 && j < j_last && j + kStepKeys <= a.S_kv) {
+                prefetch_l2(kg + (int64_t)j * ktb, (uint32_t)(kStepKeys * ktb));
+                prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)(kStepKeys * vtb));
+            }
+        };
+#pragma unroll 1
+        for (int pf = 0; pf < kPrefetchTiles / kStepTiles; ++pf) prefetch(j_first + pf * kStepKeys);
 
-        for (int s0 = r_begin + warp * kStep; s0 < r_end; s0 += kWarps * kStep) {
-            // ---- codes of this step: keys g8 and g8+8 of each tile (K),
-            //      keys 2c4, 2c4+1, 2c4+8, 2c4+9 of each tile (V)
-            uint32_t kw[kStepTiles][2][KW];
-            uint32_t vw[kStepTiles][4][VW];
-#pragma unroll
-            for (int t = 0; t < kStepTiles; ++t) {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    int j = s0 + t * kTile + g8 + 8 * r;
-                    j = min(j, a.S_kv - 1);
-                    load_codes<NKL>(kbase_g + (int64_t)j * k_tok_bytes +
-                                        (int64_t)c4 * NKL * a.kcb,
-                                    a.kcb, kw[t][r]);
-                }
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    int j = s0 + t * kTile + 2 * c4 + (r & 1) + 8 * (r >> 1);
-                    j = min(j, a.S_kv - 1);
-                    load_codes<NVL>(vbase_g + (int64_t)j * v_tok_bytes +
-                                        (int64_t)g8 * NVL * a.vcb,
-                                    a.vcb, vw[t][r]);
-                }
-            }
-            // ---- S^T = K~ Q~^T for both tiles
-            float sc[kStepTiles][4];
-#pragma unroll
-            for (int t = 0; t < kStepTiles; ++t) {
-                sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-                uint32_t af[2][KSTEPS][2];  // [row][kstep][lo/hi word]
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-#pragma unroll
-                    for (int u = 0; u < NKL; ++u) {
-                        const uint32_t code =
-                            min(code_at<NKL>(kw[t][r], a.kcb, u), (uint32_t)(a.Nk - 1));
-                        uint32_t w[4];
-                        gather<DK>(kbase + code * (uint32_t)krow, w);
-                        if constexpr (DK == 2) {
-                            af[r][u >> 1][u & 1] = w[0];
-                        } else if constexpr (DK == 4) {
-                            af[r][u][0] = w[0];
-                            af[r][u][1] = w[1];
-                        } else {
-                            af[r][2 * u][0] = w[0];
-                            af[r][2 * u][1] = w[1];
-                            af[r][2 * u + 1][0] = w[2];
-                            af[r][2 * u + 1][1] = w[3];
-                        }
-                    }
-                }
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks)
-                    mma16816(sc[t], af[0][ks][0], af[1][ks][0], af[0][ks][1],
-                             af[1][ks][1], bq[ks][0], bq[ks][1]);
-            }
-            // ---- scale, mask, online softmax (columns 2c4 and 2c4+1)
-            const bool need_mask = !(s0 >= full_lo && s0 + kStep - 1 <= full_hi);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int t = 0; t < kStepTiles; ++t) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = sc[t][e] * a.sl;
-                    if (need_mask) {
-                        const int j = s0 + t * kTile + g8 + 8 * (e >> 1);
-                        const bool ok = (e & 1) ? (j >= lo1s && j <= hi1s)
-                                                : (j >= lo0s && j <= hi0s);
-                        v = ok ? v : -INFINITY;
-                    }
-                    sc[t][e] = v;
-                }
-                mx0 = fmaxf(mx0, fmaxf(sc[t][0], sc[t][2]));
-                mx1 = fmaxf(mx1, fmaxf(sc[t][1], sc[t][3]));
-            }
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-                l0 *= al0;
-                l1 *= al1;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    acc_o[mt][0] *= al0; acc_o[mt][2] *= al0;
-                    acc_o[mt][1] *= al1; acc_o[mt][3] *= al1;
-                }
-            }
-            uint32_t bp[kStepTiles][2];
-#pragma unroll
-            for (int t = 0; t < kStepTiles; ++t) {
-                const float p0 = exp2f(sc[t][0] - mu0), p1 = exp2f(sc[t][1] - mu1);
-                const float p2 = exp2f(sc[t][2] - mu0), p3 = exp2f(sc[t][3] - mu1);
-                l0 += p0 + p2;
-                l1 += p1 + p3;
-                bp[t][0] = movmatrix_t(pack_h2(p0, p1));
-                bp[t][1] = movmatrix_t(pack_h2(p2, p3));
-            }
-            // ---- O^T += V^T P^T
-#pragma unroll
-            for (int t = 0; t < kStepTiles; ++t) {
-                // W[r][word]: value words of keys (2c4, 2c4+1, 2c4+8, 2c4+9)
-                constexpr int WPL = D / 16;   // 32-bit words per lane and key
-                uint32_t vwrd[4][WPL];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-#pragma unroll
-                    for (int u = 0; u < NVL; ++u) {
-                        const uint32_t code =
-                            min(code_at<NVL>(vw[t][r], a.vcb, u), (uint32_t)(a.Nv - 1));
-                        gather<DV>(vbase + code * (uint32_t)vrow, &vwrd[r][u * (DV / 2)]);
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const uint32_t a0 = __byte_perm(vwrd[0][mt], vwrd[1][mt], 0x5410);
-                    const uint32_t a1 = __byte_perm(vwrd[0][mt], vwrd[1][mt], 0x7632);
-                    const uint32_t a2 = __byte_perm(vwrd[2][mt], vwrd[3][mt], 0x5410);
-                    const uint32_t a3 = __byte_perm(vwrd[2][mt], vwrd[3][mt], 0x7632);
-                    mma16816(acc_o[mt], a0, a1, a2, a3, bp[t][0], bp[t][1]);
-                }
-            }
+        // ---- stream the segment, codes double-buffered in registers
+        // (a step may run past j_last by one tile; those keys belong to the
+        // next share and are masked by the per-segment bounds below)
+        us.lo_any = max(us.lo_any, j_first);
+        us.hi_any = min(us.hi_any, j_last - 1);
+        us.lo0 = max(us.lo0, j_first); us.hi0 = min(us.hi0, j_last - 1);
+        us.lo1 = max(us.lo1, j_first); us.hi1 = min(us.hi1, j_last - 1);
+        us.lo_all = max(us.lo_all, j_first); us.hi_all = min(us.hi_all, j_last - 1);
+        SC ca, cb;
+        int j = j_first;
+        load_step<D, DK, DV>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
+        while (j < j_last) {
+            if (j + kStepKeys < j_last)
+                load_step<D, DK, DV>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+            prefetch(j + kPrefetchTiles * kTile);
+            process_step<D, DK, DV, FAST>(ca, j, us, a, kbase, vbase, krow, vrow, g8, c4,
+                                          smem_raw, klane, vlane);
+            j += kStepKeys;
+            if (j >= j_last) break;
+            if (j + kStepKeys < j_last)
+                load_step<D, DK, DV>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+            prefetch(j + kPrefetchTiles * kTile);
+            process_step<D, DK, DV, FAST>(cb, j, us, a, kbase, vbase, krow, vrow, g8, c4,
+                                          smem_raw, klane, vlane);
+            j += kStepKeys;
         }
 
-        // ---- merge the warps of this CTA and write the item's partial
+        // ---- this warp's partial record for the unit
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            us.l0 += __shfl_xor_sync(0xffffffffu, us.l0, off);
+            us.l1 += __shfl_xor_sync(0xffffffffu, us.l1, off);
         }
+        float *rec = a.ws + ((gw * a.slots + slot) * kCols) * (int64_t)(D + 4);
         if (g8 == 0) {
-            sm.m[warp][2 * c4] = m0; sm.m[warp][2 * c4 + 1] = m1;
-            sm.l[warp][2 * c4] = l0; sm.l[warp][2 * c4 + 1] = l1;
+            rec[(2 * c4) * (D + 4)] = us.m0;
+            rec[(2 * c4) * (D + 4) + 1] = us.l0;
+            rec[(2 * c4 + 1) * (D + 4)] = us.m1;
+            rec[(2 * c4 + 1) * (D + 4) + 1] = us.l1;
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const int d0 = g8 * (D / 8) + 2 * mt;
-            sm.o[warp][2 * c4][d0] = acc_o[mt][0];
-            sm.o[warp][2 * c4 + 1][d0] = acc_o[mt][1];
-            sm.o[warp][2 * c4][d0 + 1] = acc_o[mt][2];
-            sm.o[warp][2 * c4 + 1][d0 + 1] = acc_o[mt][3];
+            rec[(2 * c4) * (D + 4) + 4 + d0] = us.acc_o[mt][0];
+            rec[(2 * c4 + 1) * (D + 4) + 4 + d0] = us.acc_o[mt][1];
+            rec[(2 * c4) * (D + 4) + 4 + d0 + 1] = us.acc_o[mt][2];
+            rec[(2 * c4 + 1) * (D + 4) + 4 + d0 + 1] = us.acc_o[mt][3];
         }
-        __syncthreads();
-        float *out = a.ws + item * (int64_t)kCols * (D + 4);
-        for (int idx = tid; idx < kCols * (D + 1); idx += kThreads) {
-            const int col = idx / (D + 1), d = idx % (D + 1);
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][col]);
-            const float Mu = M == -INFINITY ? 0.f : M;
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = exp2f(sm.m[w][col] - Mu);
-                acc += f * (d < D ? sm.o[w][col][d] : sm.l[w][col]);
-            }
-            float *rec = out + col * (D + 4);
-            if (d < D) rec[4 + d] = acc;
-            else { rec[0] = M; rec[1] = acc; }
-        }
+        ++slot;
+        t = seg_end;
     }
 }
 
-// Merge the splits of every (b, kv head, column block) and write fp16.
+// Merge the partial records of every (unit, column) and write fp16.
 template <int D>
 __global__ void __launch_bounds__(D)
-combine_kernel(const float *__restrict__ ws, int n_split, int n_colblk, int H_kv,
-               int H_q, int S_q, int G, __half *__restrict__ out) {
-    const int64_t unit = blockIdx.x;      // (bg, cblk)
+combine_kernel(DecArgs a, __half *__restrict__ out) {
+    const int64_t unit = blockIdx.x;
     const int col = blockIdx.y;
-    const int cblk = (int)(unit % n_colblk);
-    const int64_t bg = unit / n_colblk;
+    const int cblk = (int)(unit % a.n_colblk);
+    const int64_t bg = unit / a.n_colblk;
     const int cg = cblk * kCols + col;
-    if (cg >= G * S_q) return;
-    const int b = (int)(bg / H_kv), g = (int)(bg % H_kv);
-    const int i = cg / G, gam = cg % G;
+    if (cg >= a.G * a.S_q) return;
+    const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
+    const int i = cg / a.G, gam = cg % a.G;
     const int d = threadIdx.x;
-    const float *base = ws + (unit * n_split) * (int64_t)kCols * (D + 4) + col * (D + 4);
-    const int64_t stride = (int64_t)kCols * (D + 4);
+    const int64_t u0 = unit * a.T, u1 = u0 + a.T;
+    // first warp whose share ends after u0
+    int64_t gw = u0 * a.nw / (a.total > 0 ? a.total : 1);
+    gw = gw > 0 ? gw - 1 : 0;
+    while (gw < a.nw && share_start(gw + 1, a.total, a.nw) <= u0) ++gw;
     float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, base[s * stride]);
+    for (int64_t w = gw; w < a.nw && share_start(w, a.total, a.nw) < u1; ++w) {
+        const int64_t s = share_start(w, a.total, a.nw);
+        if (share_start(w + 1, a.total, a.nw) == s) continue;
+        const int64_t slot = unit - s / a.T;
+        M = fmaxf(M, a.ws[((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4)]);
+    }
     float o = 0.f, l = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < n_split; ++s) {
-            const float f = exp2f(base[s * stride] - M);
-            l += f * base[s * stride + 1];
-            o += f * base[s * stride + 4 + d];
+        for (int64_t w = gw; w < a.nw && share_start(w, a.total, a.nw) < u1; ++w) {
+            const int64_t s = share_start(w, a.total, a.nw);
+            if (share_start(w + 1, a.total, a.nw) == s) continue;
+            const int64_t slot = unit - s / a.T;
+            const float *rec = a.ws + ((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4);
+            const float f = exp2f(rec[0] - M);
+            l += f * rec[1];
+            o += f * rec[4 + d];
         }
         o = l > 0.f ? o / l : 0.f;
     }
-    const int hq = g * G + gam;
-    out[(((int64_t)b * H_q + hq) * S_q + i) * D + d] = __float2half_rn(o);
-}
-
-int pow2_floor(int v) {
-    int p = 1;
-    while (p * 2 <= v) p *= 2;
-    return p;
+    const int hq = g * a.G + gam;
+    out[(((int64_t)b * a.H_q + hq) * a.S_q + i) * D + d] = __float2half_rn(o);
 }
 
 struct Tables {
     int k_copies, v_copies;
+    bool fast;
     size_t bytes;
 };
 
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 210 * 1024;
 
-template <int D>
-size_t smem_struct() { return sizeof(Smem<D>); }
-
-size_t smem_struct_d(int D) {
+size_t scratch_bytes(int D) {
     switch (D) {
-        case 32: return smem_struct<32>();
-        case 64: return smem_struct<64>();
-        case 128: return smem_struct<128>();
-        default: return smem_struct<256>();
+        case 32: return warps_for(32) * sizeof(WarpScratch<32>);
+        case 64: return warps_for(64) * sizeof(WarpScratch<64>);
+        case 128: return warps_for(128) * sizeof(WarpScratch<128>);
+        default: return warps_for(256) * sizeof(WarpScratch<256>);
     }
 }
 
-// Largest replica counts (powers of two, <= 128 bytes per row) that fit.
+// Shared-memory plan: the fast path (uint8 codes, N <= 256, full replicas)
+// when it fits, else the largest replica counts (powers of two, <= 128
+// bytes per row) that fit the budget.
 Tables choose_tables(const vq_attend_args &a) {
     const int ek = 2 * a.k_sub_dim, ev = 2 * a.v_sub_dim;
+    const size_t tail = scratch_bytes(a.D) +
+                        sizeof(float) * ((size_t)a.k_n_centroids * a.k_sub_dim +
+                                         (size_t)a.v_n_centroids * a.v_sub_dim);
+    if (a.k_code_bytes == 1 && a.v_code_bytes == 1 && a.k_n_centroids <= 256 &&
+        a.v_n_centroids <= 256 && (size_t)kFastTable + tail <= kSmemBudget)
+        return {128 / ek, 128 / ev, true, (size_t)kFastTable + tail};
     int kc = 128 / ek, vc = 128 / ev;
-    const size_t base = smem_struct_d(a.D);
     auto total = [&](int k, int v) {
-        return base + (size_t)a.k_n_centroids * k * ek +
-               (size_t)a.v_n_centroids * v * ev;
+        return align16((size_t)a.k_n_centroids * k * ek) +
+               align16((size_t)a.v_n_centroids * v * ev) + tail;
     };
     while (total(kc, vc) > kSmemBudget && (kc > 1 || vc > 1)) {
         if ((size_t)a.k_n_centroids * kc * ek >= (size_t)a.v_n_centroids * vc * ev && kc > 1)
@@ -560,23 +716,22 @@ Tables choose_tables(const vq_attend_args &a) {
         else
             kc /= 2;
     }
-    return {kc, vc, total(kc, vc)};
+    return {kc, vc, false, total(kc, vc)};
 }
 
 template <int D, int DK, int DV>
-cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid,
-                     cudaStream_t stream) {
-    auto kern = decode_kernel<D, DK, DV>;
-    cudaError_t err = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tb.bytes);
+cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t stream) {
+    auto kern = tb.fast ? decode_kernel<D, DK, DV, true> : decode_kernel<D, DK, DV, false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)tb.bytes);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, tb.bytes, stream>>>(da);
+    kern<<<grid, warps_for(D) * 32, tb.bytes, stream>>>(da);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const DecArgs &da, int dk, int dv, const Tables &tb,
-                     int grid, cudaStream_t s) {
+cudaError_t launch_d(const DecArgs &da, int dk, int dv, const Tables &tb, int grid,
+                     cudaStream_t s) {
 #define VQ_CASE(K, V)                                                  \
     if (dk == K && dv == V) {                                          \
         if constexpr (K <= D / 4 && V <= D / 8)                        \
@@ -598,11 +753,19 @@ bool pair_ok(int D, int dk, int dv) {
     return listed && dk <= D / 4 && dv <= D / 8;
 }
 
-int blocks_per_sm_estimate(size_t smem) {
-    int b = (int)(227 * 1024 / (smem + 1024));
-    if (b > 8) b = 8;
-    return b < 1 ? 1 : b;
+// Common key-tile range of every unit: the union of what any query row sees.
+void tile_range(const vq_attend_args &a, int *tlo, int *T) {
+    const int q_first = a.S_kv - a.S_q, q_last = a.S_kv - 1;
+    int hi = a.causal ? q_last : a.S_kv - 1;
+    int lo = a.sliding_window > 0 ? q_first - a.sliding_window + 1 : 0;
+    if (lo < 0) lo = 0;
+    if (hi > a.S_kv - 1) hi = a.S_kv - 1;
+    if (hi < lo) { *tlo = 0; *T = 1; return; }
+    *tlo = lo / kTile;
+    *T = hi / kTile - *tlo + 1;
 }
+
+constexpr int kMinTilesPerWarp = 8;
 
 }  // namespace
 
@@ -616,64 +779,61 @@ int decode_supported(const vq_attend_args &a) {
 
 size_t decode_smem_bytes(const vq_attend_args &a) { return choose_tables(a).bytes; }
 
+// Work split: the (unit, key tile) space, units = (b, kv head, column
+// block), is cut into equal contiguous shares, one per warp of a persistent
+// grid of one CTA per SM (fewer when the problem is small).
 AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
     AttendPlan p{};
     p.cols = kCols;
     const int ncols = (a.H_q / a.H_kv) * a.S_q;
     p.n_colblk = (ncols + kCols - 1) / kCols;
+    int tlo = 0, T = 1;
+    tile_range(a, &tlo, &T);
+    p.tile_lo = tlo;
+    p.tiles = T;
     const int64_t units = (int64_t)a.B * a.H_kv * p.n_colblk;
-    const int64_t tiles = (a.S_kv + kTile - 1) / kTile;
-    const int64_t slots = (int64_t)num_sms * blocks_per_sm_estimate(choose_tables(a).bytes);
-    // pick the split count minimising (waves * tiles per split) + a per-item
-    // overhead, i.e. balance the persistent CTAs without too many partials
-    int best_n = 1;
-    double best_cost = 1e300;
-    const int max_split = (int)((tiles + 7) / 8);   // >= 128 keys per split
-    for (int n = 1; n <= 256 && n <= (max_split < 1 ? 1 : max_split); ++n) {
-        const int64_t items = units * n;
-        const int64_t waves = (items + slots - 1) / slots;
-        const int64_t tps = (tiles + n - 1) / n;
-        const double cost = (double)waves * (double)(tps + 6);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best_n = n;
-        }
-    }
-    p.n_split = best_n;
-    p.tok_per_split = (int)(((tiles + best_n - 1) / best_n) * kTile);
-    p.ws_bytes = (size_t)units * best_n * kCols * (a.D + 4) * sizeof(float);
+    p.total = units * T;
+    const int kWarps = warps_for(a.D);
+    int64_t nw = (int64_t)num_sms * kWarps;
+    const int64_t by_size = (p.total + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    if (nw > by_size) nw = by_size;
+    if (nw < 1) nw = 1;
+    p.n_warps = nw;
+    p.grid = (int)((nw + kWarps - 1) / kWarps);
+    const int64_t share = (p.total + nw - 1) / nw;
+    p.slots = (int)((share + T - 1) / T + 1);
+    p.n_split = 1;
+    p.tok_per_split = T * kTile;
+    p.ws_bytes = (size_t)nw * p.slots * kCols * (a.D + 4) * sizeof(float);
     return p;
 }
 
-AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,
-                              size_t max_ws_bytes) {
+AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms, size_t max_ws_bytes) {
     AttendPlan p = plan_decode(a, num_sms);
     if (p.ws_bytes <= max_ws_bytes) return p;
-    // fewer key splits until the partial results fit the given capacity
-    const int64_t units = (int64_t)a.B * a.H_kv * p.n_colblk;
-    const size_t per_split = (size_t)units * kCols * (a.D + 4) * sizeof(float);
-    const int64_t tiles = (a.S_kv + kTile - 1) / kTile;
-    const int64_t fit = per_split ? (int64_t)(max_ws_bytes / per_split) : 0;
-    if (fit < 1) {
-        p.n_split = 0;
-        p.ws_bytes = per_split;   // what one split alone would need
-        return p;
+    // fewer warps (longer shares) until the partial records fit
+    const size_t rec = (size_t)kCols * (a.D + 4) * sizeof(float);
+    int64_t nw = p.n_warps;
+    while (nw > 1) {
+        nw = nw / 2;
+        const int64_t share = (p.total + nw - 1) / nw;
+        const int slots = (int)((share + p.tiles - 1) / p.tiles + 1);
+        if ((size_t)nw * slots * rec <= max_ws_bytes) {
+            p.n_warps = nw;
+            p.grid = (int)((nw + warps_for(a.D) - 1) / warps_for(a.D));
+            p.slots = slots;
+            p.ws_bytes = (size_t)nw * slots * rec;
+            return p;
+        }
     }
-    const int n = (int)(fit < p.n_split ? fit : p.n_split);
-    p.n_split = n;
-    p.tok_per_split = (int)(((tiles + n - 1) / n) * kTile);
-    p.ws_bytes = per_split * (size_t)n;
+    const int64_t units = p.total / p.tiles;
+    p.n_split = 0;
+    p.ws_bytes = (size_t)(units + 1) * rec;   // what a single warp would need
     return p;
 }
 
 cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
                           cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaError_t err;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) !=
-        cudaSuccess)
-        return err;
     const Tables tb = choose_tables(a);
     DecArgs da{};
     da.B = a.B; da.H_q = a.H_q; da.H_kv = a.H_kv; da.S_q = a.S_q; da.S_kv = a.S_kv;
@@ -694,36 +854,31 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.causal = a.causal;
     da.window = a.sliding_window;
     da.ws = reinterpret_cast<float *>(a.workspace);
-    da.n_split = plan.n_split;
     da.n_colblk = plan.n_colblk;
-    da.tiles_per_split = plan.tok_per_split / kTile;
-    da.n_items = (int64_t)a.B * a.H_kv * plan.n_colblk * plan.n_split;
+    da.tlo = plan.tile_lo;
+    da.T = plan.tiles;
+    da.total = plan.total;
+    da.nw = (int)plan.n_warps;
+    da.slots = plan.slots;
     da.k_copies = tb.k_copies;
     da.v_copies = tb.v_copies;
-    int per_sm = 1;
-    int64_t grid = 0;
-    {
-        // occupancy of the instantiated kernel decides the persistent grid
-        per_sm = blocks_per_sm_estimate(tb.bytes);
-        grid = (int64_t)sms * per_sm;
-        if (grid > da.n_items) grid = da.n_items;
-        if (grid < 1) grid = 1;
-    }
+    cudaError_t err;
     switch (a.D) {
-        case 32: err = launch_d<32>(da, a.k_sub_dim, a.v_sub_dim, tb, (int)grid, stream); break;
-        case 64: err = launch_d<64>(da, a.k_sub_dim, a.v_sub_dim, tb, (int)grid, stream); break;
-        case 128: err = launch_d<128>(da, a.k_sub_dim, a.v_sub_dim, tb, (int)grid, stream); break;
-        case 256: err = launch_d<256>(da, a.k_sub_dim, a.v_sub_dim, tb, (int)grid, stream); break;
+        case 32: err = launch_d<32>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
+        case 64: err = launch_d<64>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
+        case 128: err = launch_d<128>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
+        case 256: err = launch_d<256>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess) return err;
-    const int64_t units = (int64_t)a.B * a.H_kv * plan.n_colblk;
+    const int64_t units = plan.total / plan.tiles;
     dim3 cgrid((unsigned)units, kCols);
+    __half *out = reinterpret_cast<__half *>(a.out_f16);
     switch (a.D) {
-        case 32: combine_kernel<32><<<cgrid, 32, 0, stream>>>(da.ws, plan.n_split, plan.n_colblk, a.H_kv, a.H_q, a.S_q, da.G, reinterpret_cast<__half *>(a.out_f16)); break;
-        case 64: combine_kernel<64><<<cgrid, 64, 0, stream>>>(da.ws, plan.n_split, plan.n_colblk, a.H_kv, a.H_q, a.S_q, da.G, reinterpret_cast<__half *>(a.out_f16)); break;
-        case 128: combine_kernel<128><<<cgrid, 128, 0, stream>>>(da.ws, plan.n_split, plan.n_colblk, a.H_kv, a.H_q, a.S_q, da.G, reinterpret_cast<__half *>(a.out_f16)); break;
-        default: combine_kernel<256><<<cgrid, 256, 0, stream>>>(da.ws, plan.n_split, plan.n_colblk, a.H_kv, a.H_q, a.S_q, da.G, reinterpret_cast<__half *>(a.out_f16)); break;
+        case 32: combine_kernel<32><<<cgrid, 32, 0, stream>>>(da, out); break;
+        case 64: combine_kernel<64><<<cgrid, 64, 0, stream>>>(da, out); break;
+        case 128: combine_kernel<128><<<cgrid, 128, 0, stream>>>(da, out); break;
+        default: combine_kernel<256><<<cgrid, 256, 0, stream>>>(da, out); break;
     }
     return cudaGetLastError();
 }

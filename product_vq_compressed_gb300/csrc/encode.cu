@@ -10,17 +10,21 @@
 //                                 registers, one index per sub-vector;
 //   vecinfer_dequant_metal        codebook gather.
 //
-// GB300 layout.  A block of 256 threads stages the whole codebook (fp32) in
+// GB300 layout.  A block of 128 threads stages the whole codebook (fp32) in
 // shared memory once and then walks a persistent loop over tiles of 512
 // sub-vectors (512 / n_sub tokens):
 //   1. one warp per token: fp16 load (8-byte vectors, coalesced), smooth and
 //      1/sqrt(D) folded into the load, in-place FWHT in shared memory;
-//   2. every thread owns two sub-vectors and scans the codebook; all threads
+//   2. every thread owns four sub-vectors and scans the codebook; all threads
 //      read the same centroid at the same time, so each shared-memory read
-//      is a broadcast, and one centroid load serves both sub-vectors;
-//      fp32 direct-form distances sum_t (y_t - c_t)^2, strict '<' keeps the
-//      lowest index on ties; codes are written in sub-vector order
-//      (coalesced uint8 / uint16 stores);
+//      is a broadcast, and one centroid load serves all four.  The
+//      scan screens with f_c = |c|^2 - 2 y.c (one fused multiply-add per
+//      dimension; -2c and |c|^2 are staged once), tracking the best and the
+//      second-best value; strict '<' keeps the lowest index on ties.  If
+//      the two are closer than twice a rigorous bound on the fp32 error of
+//      that form, the sub-vector is rescanned with the direct form
+//      sum_t (y_t - c_t)^2, so every decision is the one the direct form
+//      makes.  Codes are written in sub-vector order (coalesced stores);
 //   3. optional reconstruction: the chosen centroids replace the sub-vectors
 //      in shared memory, one warp per token runs the FWHT again (Hn is
 //      symmetric and its own inverse), divides by the smooth factors and
@@ -34,8 +38,9 @@
 namespace vqkv {
 namespace {
 
-constexpr int kEncThreads = 256;
-constexpr int kSlots = 512;  // sub-vectors per tile (two per thread)
+constexpr int kEncThreads = 128;
+constexpr int kSlots = 512;  // sub-vectors per tile
+constexpr int kR = kSlots / kEncThreads;  // sub-vectors per thread
 
 // Unnormalised in-place Walsh-Hadamard transform (natural order) of the D
 // floats at v, by one warp.  Butterfly at stride h pairs i and i + h.
@@ -73,10 +78,25 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
     extern __shared__ __align__(16) float smem[];
     const int N = p.N, D = p.D;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // shared memory: -2c [N][SUBD], |c|^2 [N], max |c|^2, sub-vectors [512][SUBD]
     float *cb_s = smem;
-    float *y_s = smem + ((N * SUBD + 3) & ~3);
+    float *nrm_s = cb_s + ((N * SUBD + 3) & ~3);
+    float *maxn2_s = nrm_s + ((N + 3) & ~3);
+    float *y_s = maxn2_s + 4;
 
-    for (int i = tid; i < N * SUBD; i += kEncThreads) cb_s[i] = p.codebook[i];
+    if (tid == 0) *maxn2_s = 0.f;
+    for (int i = tid; i < N * SUBD; i += kEncThreads) cb_s[i] = -2.0f * p.codebook[i];
+    __syncthreads();
+    for (int c = tid; c < N; c += kEncThreads) {
+        float n2 = 0.f;
+        for (int t = 0; t < SUBD; ++t) {
+            const float v = p.codebook[c * SUBD + t];
+            n2 = fmaf(v, v, n2);
+        }
+        nrm_s[c] = n2;
+        // non-negative floats order like their bit patterns
+        atomicMax(reinterpret_cast<int *>(maxn2_s), __float_as_int(n2));
+    }
     __syncthreads();
 
     const int n_sub = D / SUBD;
@@ -118,38 +138,69 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
         }
         __syncthreads();
 
-        // ---- 2. nearest centroid of two sub-vectors per thread
+        // ---- 2. nearest centroid of kR sub-vectors per thread
         {
-            const int s0 = tid, s1 = tid + kEncThreads;
-            float y0[SUBD], y1[SUBD];
-            load_sub<SUBD>(y_s + s0 * SUBD, y0);
-            load_sub<SUBD>(y_s + s1 * SUBD, y1);
-            float best0 = INFINITY, best1 = INFINITY;
-            int bi0 = 0, bi1 = 0;
-#pragma unroll 4
+            float y[kR][SUBD];
+#pragma unroll
+            for (int r = 0; r < kR; ++r) load_sub<SUBD>(y_s + (tid + r * kEncThreads) * SUBD, y[r]);
+            // screening in the expanded form f_c = |c|^2 - 2 y.c (one fused
+            // multiply-add per dimension), keeping the best and second best
+            float f1[kR], f2[kR];
+            int i1[kR];
+#pragma unroll
+            for (int r = 0; r < kR; ++r) { f1[r] = INFINITY; f2[r] = INFINITY; i1[r] = 0; }
+#pragma unroll 2
             for (int c = 0; c < N; ++c) {
                 float cv[SUBD];
                 load_sub<SUBD>(cb_s + c * SUBD, cv);
-                float d0 = 0.f, d1 = 0.f;
+                const float nc = nrm_s[c];
 #pragma unroll
-                for (int t = 0; t < SUBD; ++t) {
-                    const float e0 = y0[t] - cv[t];
-                    const float e1 = y1[t] - cv[t];
-                    d0 = fmaf(e0, e0, d0);
-                    d1 = fmaf(e1, e1, d1);
+                for (int r = 0; r < kR; ++r) {
+                    float f = nc;
+#pragma unroll
+                    for (int t = 0; t < SUBD; ++t) f = fmaf(cv[t], y[r][t], f);
+                    f2[r] = fminf(f2[r], fmaxf(f1[r], f));
+                    const bool lt = f < f1[r];
+                    i1[r] = lt ? c : i1[r];
+                    f1[r] = fminf(f1[r], f);
                 }
-                if (d0 < best0) { best0 = d0; bi0 = c; }
-                if (d1 < best1) { best1 = d1; bi1 = c; }
             }
-            const int64_t g0 = v0 * n_sub + s0, g1 = v0 * n_sub + s1;
-            const int64_t lim = p.n_vec * n_sub;
-            if (g0 < lim) codes[g0] = (CodeT)bi0;
-            if (g1 < lim) codes[g1] = (CodeT)bi1;
-            if (p.xhat) {
+            // When the two best screened values are closer than twice the
+            // fp32 error bound of the expanded form, order them exactly:
+            // rescan with the direct form sum_t (y_t - c_t)^2 (c = -cb/2).
+            const float maxn2 = *maxn2_s;
 #pragma unroll
-                for (int t = 0; t < SUBD; ++t) {
-                    y_s[s0 * SUBD + t] = cb_s[bi0 * SUBD + t];
-                    y_s[s1 * SUBD + t] = cb_s[bi1 * SUBD + t];
+            for (int r = 0; r < kR; ++r) {
+                float ny2 = 0.f;
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t) ny2 = fmaf(y[r][t], y[r][t], ny2);
+                const float bound = (4.0f * SUBD + 8.0f) * 5.9604645e-8f *
+                                    (maxn2 + 2.0f * sqrtf(maxn2 * ny2) + 1e-30f);
+                if (f2[r] - f1[r] <= 2.0f * bound) {
+                    float best = INFINITY;
+                    int bi = 0;
+                    for (int c = 0; c < N; ++c) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int t = 0; t < SUBD; ++t) {
+                            const float e = y[r][t] + 0.5f * cb_s[c * SUBD + t];
+                            d = fmaf(e, e, d);
+                        }
+                        if (d < best) { best = d; bi = c; }
+                    }
+                    i1[r] = bi;
+                }
+            }
+            const int64_t lim = p.n_vec * n_sub;
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int sl = tid + r * kEncThreads;
+                const int64_t gi = v0 * n_sub + sl;
+                if (gi < lim) codes[gi] = (CodeT)i1[r];
+                if (p.xhat) {
+#pragma unroll
+                    for (int t = 0; t < SUBD; ++t)
+                        y_s[sl * SUBD + t] = -0.5f * cb_s[i1[r] * SUBD + t];
                 }
             }
         }
@@ -245,6 +296,7 @@ cudaError_t launch_encode_c(const EncodeParams &p, cudaStream_t s) {
 
 size_t encode_smem_bytes(int N, int sub_dim) {
     return sizeof(float) * ((((size_t)N * sub_dim + 3) & ~(size_t)3) +
+                            (((size_t)N + 3) & ~(size_t)3) + 4 +
                             (size_t)kSlots * sub_dim);
 }
 

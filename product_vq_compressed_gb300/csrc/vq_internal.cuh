@@ -43,11 +43,16 @@ cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- attend
 struct AttendPlan {
-    int n_split;        // key-axis splits per (b, kv head, column block)
+    int n_split;        // 1 (0 when a capped plan cannot fit)
     int cols;           // query columns (head, row) pairs per column block
     int n_colblk;       // column blocks per (b, kv head)
-    int tok_per_split;  // keys per split (multiple of the tile)
-    size_t ws_bytes;    // partial results
+    int tok_per_split;  // keys each unit scans
+    int tile_lo, tiles; // every unit scans key tiles [tile_lo, tile_lo + tiles)
+    int64_t total;      // units * tiles
+    int64_t n_warps;    // warps sharing the flattened work
+    int grid;           // CTAs
+    int slots;          // partial records per warp
+    size_t ws_bytes;    // partial records
 };
 AttendPlan plan_decode(const vq_attend_args &a, int num_sms);
 // The same plan with at most max_ws_bytes of partial results (fewer key
