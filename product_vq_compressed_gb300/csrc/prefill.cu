@@ -1,19 +1,501 @@
-// prefill.cu -- tensor-core (tcgen05) attention over the coded cache for
-// long query blocks.  Not built yet: every request is served by the split-KV
-// path.
+// prefill.cu -- attention over the coded cache for long query blocks on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Page: "Metal Kernels API", section "Fused SDPA", metal_fused_sdpa (SDPA on
+// the dequantised cache without materialising it; causal alignment to the
+// tail of the cache; sliding window; GQA), with the raw-query semantics of
+// VecInferKVCache.fused_sdpa; the prefill-shaped loop over key tiles follows
+// the companion kernel described under rabitq_prefill_attend (both products
+// on matrix tiles, keys and values decoded inside the tile loop).
+//
+// One CTA = (batch, query head, tile of 128 query rows); thread i owns query
+// row i, which is also tensor-memory lane i of every accumulator.
+//   * Q~ = Hn (q (.) s_g^-1) * scale * log2(e) is built once per CTA (FWHT in
+//     registers) and stored as the A operand in the canonical K-major,
+//     128-byte-swizzled shared-memory layout (fp16).
+//   * For every tile of 128 keys the CTA rebuilds, from the uint8 codes and
+//     fp16 codebook replicas in shared memory, K~ [keys x D] (B operand of
+//     S = Q~ K~^T) and V_hat^T [D x keys] (B operand of O = P V_hat), both
+//     K-major and swizzled.
+//   * One thread issues tcgen05.mma (kind::f16, M = N = 128, K = 16 per
+//     instruction, fp32 accumulate) into tensor memory and commits to an
+//     mbarrier; every thread reads its row back with tcgen05.ld.
+//   * Online softmax in base 2 per row: a max pass and an exp pass over the
+//     score row in tensor memory; P (fp16) goes to shared memory as the A
+//     operand of the second product; the running output stays in registers
+//     (O = O * alpha + P V_hat per tile).
+//   * Key tiles that no row of the CTA can see are skipped; masks are applied
+//     only on tiles that need them.
+// Every mbarrier wait is bounded: if one expires the CTA writes NaN rows,
+// waits (bounded) for its own MMAs once more, frees its tensor memory and
+// exits, so a fault shows up in the output instead of hanging the GPU.
+#include <math.h>
+
 #include "vq_internal.cuh"
 
 namespace vqkv {
+namespace {
+
+constexpr int kRows = 128;        // query rows per CTA (MMA M)
+constexpr int kKeys = 128;        // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kD = 128;           // head dimension of this kernel
+constexpr int kThreads = 128;
+constexpr int kSub = 4;           // sub-vector size of both codebooks
+constexpr uint32_t kTileBytes = kRows * kD * 2;  // one fp16 operand tile, 32 KiB
+constexpr uint32_t kHalfTile = kTileBytes / 2;   // 64-element K half, 16 KiB
+constexpr uint32_t kTabBytes = 256 * 256;        // interleaved K | V replicas
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+
+// Bounded wait for phase `parity` of the mbarrier; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused when swizzled)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // version
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
+// M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kKeys >> 3) << 17) |
+                            ((uint32_t)(kRows >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+        ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (8 fp16 along K) of row `row` in a
+// K-major operand tile made of two 64-element K halves of [128 rows x 128 B]
+// with the 128-byte swizzle (chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
+    const int half = chunk >> 3, c = chunk & 7;
+    return (uint32_t)(half * kHalfTile + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+struct PrefillArgs {
+    int B, H_q, H_kv, S_q, S_kv, G;
+    const __half *q;
+    const uint8_t *kc, *vc;       // uint8 codes, 32 per key
+    const float *kcb, *vcb;       // [Nk, 4], [Nv, 4] fp32
+    int Nk, Nv;
+    const float *smooth;
+    int smooth_mode;
+    float qscale;                 // scale * log2(e) / sqrt(D), folded into Q~
+    int causal, window;
+    __half *out;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat^T | P | tables | misc
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base, sK = base + kTileBytes, sV = base + 2 * kTileBytes,
+                   sP = base + 3 * kTileBytes, sTab = base + 4 * kTileBytes;
+    unsigned char *tab = gbase + 4 * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 4 * kTileBytes + kTabBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+    const int g = hq / a.G;
+    const int q0 = qt * kRows;
+    const int row = q0 + tid;              // this thread's query row
+    const bool row_ok = row < a.S_q;
+
+    // ---- tensor memory: S in columns [0, 128), P V_hat in [128, 256)
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                     ::"r"(smem_u32(tmem_slot)), "r"(256));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+
+    // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16
+    for (int i = tid; i < 256 * 64; i += kThreads) {
+        const int c = i >> 6, w = i & 63;            // 64 words per 256-byte row
+        const bool is_v = w >= 32;
+        const int t = (w & 1) * 2;                   // dims (t, t+1) of the centroid
+        const int n = is_v ? a.Nv : a.Nk;
+        const float *cb = is_v ? a.vcb : a.kcb;
+        reinterpret_cast<uint32_t *>(tab)[i] =
+            c < n ? pack_h2(cb[c * kSub + t], cb[c * kSub + t + 1]) : 0u;
+    }
+
+    // ---- Q~ row of this thread (fp16, swizzled A operand)
+    {
+        float x[kD];
+        if (row_ok) {
+            const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD;
+            const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
+#pragma unroll
+            for (int e = 0; e < kD; e += 8) {
+                const uint4 raw4 = *reinterpret_cast<const uint4 *>(qp + e);
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __half22float2(h2[k]);
+                    x[e + 2 * k] = f.x;
+                    x[e + 2 * k + 1] = f.y;
+                }
+            }
+            if (a.smooth_mode != 0) {
+#pragma unroll
+                for (int e = 0; e < kD; ++e) x[e] = x[e] / sp[e];
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kD; ++e) x[e] = 0.f;
+        }
+#pragma unroll
+        for (int h = 1; h < kD; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < kD; ++i) {
+                if ((i & h) == 0) {
+                    const float u = x[i], v = x[i + h];
+                    x[i] = u + v;
+                    x[i + h] = u - v;
+                }
+            }
+        }
+#pragma unroll
+        for (int ch = 0; ch < kD / 8; ++ch) {
+            const float *p = x + ch * 8;
+            sts128(sQ + sw_off(tid, ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
+                   pack_h2(p[2] * a.qscale, p[3] * a.qscale),
+                   pack_h2(p[4] * a.qscale, p[5] * a.qscale),
+                   pack_h2(p[6] * a.qscale, p[7] * a.qscale));
+        }
+    }
+
+    // ---- visible keys of this row and of the CTA
+    const int q_abs = a.S_kv - a.S_q + row;
+    int hi = a.causal ? q_abs : a.S_kv - 1;
+    hi = min(hi, a.S_kv - 1);
+    int lo = a.window > 0 ? max(0, q_abs - a.window + 1) : 0;
+    if (!row_ok) { lo = 1; hi = 0; }
+    const int last_row = min(q0 + kRows, a.S_q) - 1;
+    const int qa_first = a.S_kv - a.S_q + q0, qa_last = a.S_kv - a.S_q + last_row;
+    const int cta_lo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
+    const int cta_hi = min(a.causal ? qa_last : a.S_kv - 1, a.S_kv - 1);
+    const int all_lo = a.window > 0 ? max(0, qa_last - a.window + 1) : 0;   // seen by every row
+    const int all_hi = min(a.causal ? qa_first : a.S_kv - 1, a.S_kv - 1);
+    const int t_first = cta_lo / kKeys, t_last = cta_hi / kKeys;
+
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_o = t_s + kKeys;
+
+    float o[kD];
+#pragma unroll
+    for (int e = 0; e < kD; ++e) o[e] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    uint32_t ph_s = 0, ph_o = 0;
+    bool failed = false;
+
+    const int64_t bg = (int64_t)b * a.H_kv + g;
+    const uint8_t *kcodes = a.kc + bg * a.S_kv * 32;
+    const uint8_t *vcodes = a.vc + bg * a.S_kv * 32;
+    const int vm = tid & 31, vk = (tid >> 5) * 32;   // value sub-vector column, key block
+
+    for (int tile = t_first; tile <= t_last && !failed; ++tile) {
+        const int j0 = tile * kKeys;
+        // ---- K~ row `tid` of the tile: 32 centroids of key j0 + tid
+        {
+            const int j = min(j0 + tid, a.S_kv - 1);
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const uint32_t lane_off = (uint32_t)((tid & 15) * 8);
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {   // chunk = two centroids = 8 dims
+                const uint32_t w = cw[ch >> 1];
+                const int i0 = (ch & 1) * 2;
+                const uint2 e0 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i0 << 4)));
+                const uint2 e1 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)(i0 + 1) << 4)));
+                sts128(sK + sw_off(tid, ch), e0.x, e0.y, e1.x, e1.y);
+            }
+        }
+        // ---- V_hat^T: dims 4vm..4vm+3 of keys j0+vk .. j0+vk+31
+        {
+            uint32_t lo_w[32], hi_w[32];   // dims (0,1) and (2,3) per key
+            const uint32_t lane_off = 128u + (uint32_t)((tid & 15) * 8);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int j = min(j0 + vk + k, a.S_kv - 1);
+                const uint32_t code = vcodes[(int64_t)j * 32 + vm];
+                const uint2 e = lds64(sTab + (code << 8) + lane_off);
+                lo_w[k] = e.x;
+                hi_w[k] = e.y;
+            }
+            // rows 4vm + i, keys vk + 8q .. vk + 8q + 7 -> chunk (vk / 8 + q)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r0[4], r1[4], r2[4], r3[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int k = 8 * q + 2 * p;
+                    r0[p] = __byte_perm(lo_w[k], lo_w[k + 1], 0x5410);
+                    r1[p] = __byte_perm(lo_w[k], lo_w[k + 1], 0x7632);
+                    r2[p] = __byte_perm(hi_w[k], hi_w[k + 1], 0x5410);
+                    r3[p] = __byte_perm(hi_w[k], hi_w[k + 1], 0x7632);
+                }
+                const int ch = vk / 8 + q;
+                sts128(sV + sw_off(4 * vm + 0, ch), r0[0], r0[1], r0[2], r0[3]);
+                sts128(sV + sw_off(4 * vm + 1, ch), r1[0], r1[1], r1[2], r1[3]);
+                sts128(sV + sw_off(4 * vm + 2, ch), r2[0], r2[1], r2[2], r2[3]);
+                sts128(sV + sw_off(4 * vm + 3, ch), r3[0], r3[1], r3[2], r3[3]);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // ---- S = Q~ K~^T into tensor memory
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
+                mma_f16(tmem, smem_desc(sQ + off), smem_desc(sK + off), ks > 0);
+            }
+            mma_commit(bar_s);
+        }
+        // every thread waits (bounded); the verdict is made uniform so that
+        // no thread can leave the loop while others sit in a barrier
+        if (__syncthreads_or(!mbar_wait(bar_s, ph_s))) { failed = true; break; }
+        ph_s ^= 1;
+        tc_fence_after();
+
+        // ---- online softmax of row `tid` over this tile
+        const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) {
+            float s[32];
+            tmem_ld32(t_s + c * 32, s);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = j0 + c * 32 + i;
+                const float v = (full || (j >= lo && j <= hi)) ? s[i] : -INFINITY;
+                mx = fmaxf(mx, v);
+            }
+        }
+        const float m_new = fmaxf(m, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2(m - m_use);
+        m = m_new;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) {
+            float s[32];
+            tmem_ld32(t_s + c * 32, s);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int j = j0 + c * 32 + i;
+                const float p0 = (full || (j >= lo && j <= hi)) ? ex2(s[i] - m_use) : 0.f;
+                const float p1 = (full || (j + 1 >= lo && j + 1 <= hi)) ? ex2(s[i + 1] - m_use) : 0.f;
+                lsum += p0 + p1;
+                pk[i / 2] = pack_h2(p0, p1);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                sts128(sP + sw_off(tid, c * 4 + q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                       pk[4 * q + 3]);
+        }
+        l = l * alpha + lsum;
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // ---- P V_hat into tensor memory
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+                const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
+                mma_f16(tmem + kKeys, smem_desc(sP + off), smem_desc(sV + off), ks > 0);
+            }
+            mma_commit(bar_o);
+        }
+        if (__syncthreads_or(!mbar_wait(bar_o, ph_o))) { failed = true; break; }
+        ph_o ^= 1;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+            float pv[32];
+            tmem_ld32(t_o + c * 32, pv);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, pv[i]);
+        }
+        tc_fence_before();
+        __syncthreads();   // K~, V_hat^T, P and tensor memory are reused next tile
+    }
+
+    // ---- output row
+    if (row_ok) {
+        __half *op = a.out + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD;
+        const float inv = failed ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
+#pragma unroll
+        for (int ch = 0; ch < kD / 8; ++ch) {
+            const float *p = o + ch * 8;
+            uint4 v;
+            v.x = pack_h2(p[0] * inv, p[1] * inv);
+            v.y = pack_h2(p[2] * inv, p[3] * inv);
+            v.z = pack_h2(p[4] * inv, p[5] * inv);
+            v.w = pack_h2(p[6] * inv, p[7] * inv);
+            *reinterpret_cast<uint4 *>(op + ch * 8) = v;
+        }
+    }
+    if (failed) {   // let any MMA still in flight finish before freeing its memory
+        mbar_wait(bar_s, ph_s);
+        mbar_wait(bar_o, ph_o);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n"
+                     ::"r"(tmem), "r"(256));
+    }
+}
+
+size_t prefill_smem_bytes() {
+    return 4 * (size_t)kTileBytes + kTabBytes + 64 + 1024;   // + alignment slack
+}
+
+}  // namespace
 
 int prefill_supported(const vq_attend_args &a) {
-    (void)a;
-    return VQ_ERR_UNSUPPORTED;
+    if (a.D != kD || a.k_sub_dim != kSub || a.v_sub_dim != kSub) return VQ_ERR_UNSUPPORTED;
+    if (a.k_code_bytes != 1 || a.v_code_bytes != 1) return VQ_ERR_UNSUPPORTED;
+    if (a.k_n_centroids > 256 || a.v_n_centroids > 256) return VQ_ERR_UNSUPPORTED;
+    if (a.S_q < 64) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
 }
 
 cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream) {
-    (void)a;
-    (void)stream;
-    return cudaErrorNotSupported;
+    PrefillArgs p{};
+    p.B = a.B; p.H_q = a.H_q; p.H_kv = a.H_kv; p.S_q = a.S_q; p.S_kv = a.S_kv;
+    p.G = a.H_q / a.H_kv;
+    p.q = reinterpret_cast<const __half *>(a.q_f16);
+    p.kc = reinterpret_cast<const uint8_t *>(a.k_codes);
+    p.vc = reinterpret_cast<const uint8_t *>(a.v_codes);
+    p.kcb = a.k_codebook;
+    p.vcb = a.v_codebook;
+    p.Nk = a.k_n_centroids;
+    p.Nv = a.v_n_centroids;
+    p.smooth = a.smooth;
+    p.smooth_mode = a.smooth_mode;
+    p.qscale = (float)((double)a.scale * 1.4426950408889634 / sqrt((double)kD));
+    p.causal = a.causal;
+    p.window = a.sliding_window;
+    p.out = reinterpret_cast<__half *>(a.out_f16);
+    const size_t smem = prefill_smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(prefill_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)((a.S_q + kRows - 1) / kRows), (unsigned)a.H_q, (unsigned)a.B);
+    prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace vqkv
