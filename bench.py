@@ -251,6 +251,10 @@ def run_gpu(args, name, rank, world):
         wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
+    out_t = r.d["k_codes"] if name == "bulk-encode" else r.d["out"]
+    finite = bool(torch.isfinite(out_t.float()).all()) if out_t.is_floating_point() else True
+    if not finite:
+        print("warning: non-finite values in the step's output", file=sys.stderr)
     step_ms = [evs[k][0].elapsed_time(evs[k][2]) for k in range(K)]
     dom_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(K)]
     total_s = sum(step_ms) / 1e3
@@ -317,7 +321,7 @@ def run_gpu(args, name, rank, world):
                    "sliding_window": spec.window, "l2": "flushed before every timed step",
                    "parallelism": f"replicas x{world}"},
         "e2e": e2e, "gpu_launches": launches, "roofline": roof, "clocks": clocks,
-        "wall_s_timed_region": round(wall, 4),
+        "wall_s_timed_region": round(wall, 4), "output_finite": finite,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(name, spec, inp, budget_s=args.cpu_budget)

@@ -14,9 +14,9 @@
 //     registers) and stored as the A operand in the canonical K-major,
 //     128-byte-swizzled shared-memory layout (fp16).
 //   * For every tile of 128 keys the CTA rebuilds, from the uint8 codes and
-//     fp16 codebook replicas in shared memory, K~ [keys x D] (B operand of
-//     S = Q~ K~^T) and V_hat^T [D x keys] (B operand of O = P V_hat), both
-//     K-major and swizzled.
+//     fp16 codebook replicas in shared memory, K~ and V_hat as [keys x D]
+//     tiles (one key row per thread, 128-byte swizzle): K~ is the K-major B
+//     operand of S = Q~ K~^T, V_hat the MN-major B operand of O = P V_hat.
 //   * One thread issues tcgen05.mma (kind::f16, M = N = 128, K = 16 per
 //     instruction, fp32 accumulate) into tensor memory and commits to an
 //     mbarrier; every thread reads its row back with tcgen05.ld.
@@ -26,6 +26,10 @@
 //     (O = O * alpha + P V_hat per tile).
 //   * Key tiles that no row of the CTA can see are skipped; masks are applied
 //     only on tiles that need them.
+//   * Pipelining: while the tensor cores compute Q~K~^T of tile j, the codes
+//     of tile j+1 load into registers; while they compute P V_hat of tile j,
+//     the threads rebuild K~ and V_hat of tile j+1 (V_hat double buffered).  One thread polls each mbarrier; the others wait at the
+//     block barrier that follows.
 // Every mbarrier wait is bounded: if one expires the CTA writes NaN rows,
 // waits (bounded) for its own MMAs once more, frees its tensor memory and
 // exits, so a fault shows up in the output instead of hanging the GPU.
@@ -91,17 +95,31 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
-// M = 128, N = 128.
+// Shared-memory matrix descriptor for an MN-major operand with the 128-byte
+// swizzle: 64 MN elements (128 bytes) per row, one row per K index, 8-row
+// groups 1024 bytes apart (stride byte offset, along K), 64-element MN
+// blocks `mn_stride` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptors, kind::f16: fp16 A and B, fp32 D, M = 128,
+// N = 128; A K-major; B K-major (S = Q~ K~^T) or MN-major (O = P V_hat).
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kKeys >> 3) << 17) |
                             ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdescBmn = kIdesc | (1u << 16);
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t accumulate) {
+                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -175,14 +193,14 @@ struct PrefillArgs {
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat^T | P | tables | misc
+    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat x2 | P | tables | misc
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t sQ = base, sK = base + kTileBytes, sV = base + 2 * kTileBytes,
-                   sP = base + 3 * kTileBytes, sTab = base + 4 * kTileBytes;
-    unsigned char *tab = gbase + 4 * kTileBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 4 * kTileBytes + kTabBytes);
+                   sP = base + 4 * kTileBytes, sTab = base + 5 * kTileBytes;
+    unsigned char *tab = gbase + 5 * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 5 * kTileBytes + kTabBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
 
@@ -206,12 +224,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     }
 
     // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16
+    //      (fp32 codebooks first copied into the P region with coalesced loads)
+    float *stage = reinterpret_cast<float *>(gbase + 4 * kTileBytes);
+    for (int i = tid; i < a.Nk * kSub; i += kThreads) stage[i] = a.kcb[i];
+    for (int i = tid; i < a.Nv * kSub; i += kThreads) stage[1024 + i] = a.vcb[i];
+    __syncthreads();
     for (int i = tid; i < 256 * 64; i += kThreads) {
         const int c = i >> 6, w = i & 63;            // 64 words per 256-byte row
         const bool is_v = w >= 32;
         const int t = (w & 1) * 2;                   // dims (t, t+1) of the centroid
         const int n = is_v ? a.Nv : a.Nk;
-        const float *cb = is_v ? a.vcb : a.kcb;
+        const float *cb = stage + (is_v ? 1024 : 0);
         reinterpret_cast<uint32_t *>(tab)[i] =
             c < n ? pack_h2(cb[c * kSub + t], cb[c * kSub + t + 1]) : 0u;
     }
@@ -276,14 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     const int all_hi = min(a.causal ? qa_first : a.S_kv - 1, a.S_kv - 1);
     const int t_first = cta_lo / kKeys, t_last = cta_hi / kKeys;
 
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t t_o = t_s + kKeys;
-
     float o[kD];
 #pragma unroll
     for (int e = 0; e < kD; ++e) o[e] = 0.f;
@@ -294,88 +309,101 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     const int64_t bg = (int64_t)b * a.H_kv + g;
     const uint8_t *kcodes = a.kc + bg * a.S_kv * 32;
     const uint8_t *vcodes = a.vc + bg * a.S_kv * 32;
-    const int vm = tid & 31, vk = (tid >> 5) * 32;   // value sub-vector column, key block
 
-    for (int tile = t_first; tile <= t_last && !failed; ++tile) {
+    // codes of one tile in registers: key row `tid`, K and V side
+    uint32_t kcw[8], vcw[8];
+    auto load_codes = [&](int j0) {
+        const int j = min(j0 + tid, a.S_kv - 1);
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
+        const uint4 d0 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32);
+        const uint4 d1 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32 + 16);
+        kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
+        kcw[4] = c1.x; kcw[5] = c1.y; kcw[6] = c1.z; kcw[7] = c1.w;
+        vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
+        vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
+    };
+    // Row `tid` (the tile's key `tid`) of a [keys x D] fp16 tile: 32
+    // centroids, two per 16-byte chunk, 128-byte swizzle.  The same image
+    // serves as K~ (B of Q~K~^T, K-major) and as V_hat (B of P V_hat, read
+    // MN-major: keys along K, dims contiguous).
+    auto build_rows = [&](const uint32_t *cw, uint32_t dst, uint32_t half_off) {
+        const uint32_t lane_off = half_off + (uint32_t)((tid & 15) * 8);
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+            const uint32_t w = cw[ch >> 1];
+            const int i0 = (ch & 1) * 2;
+            const uint2 e0 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i0 << 4)));
+            const uint2 e1 =
+                lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)(i0 + 1) << 4)));
+            sts128(dst + sw_off(tid, ch), e0.x, e0.y, e1.x, e1.y);
+        }
+    };
+    auto build_k = [&]() { build_rows(kcw, sK, 0u); };
+    auto build_v = [&](uint32_t sVb) { build_rows(vcw, sVb, 128u); };
+
+    // ---- first tile's operands, then the pipelined loop:
+    //   QK(j) on the tensor cores   || codes of tile j+1 loading
+    //   softmax(j) -> P
+    //   PV(j) on the tensor cores   || K~(j+1), V_hat(j+1) rebuilt
+    //   O = O * alpha + PV(j)
+    if (t_first <= t_last) {
+        load_codes(t_first * kKeys);
+        build_k();
+        build_v(sV + (uint32_t)(t_first & 1) * kTileBytes);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_o = t_s + kKeys;
+
+    for (int tile = t_first; tile <= t_last; ++tile) {
         const int j0 = tile * kKeys;
-        // ---- K~ row `tid` of the tile: 32 centroids of key j0 + tid
-        {
-            const int j = min(j0 + tid, a.S_kv - 1);
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            const uint32_t lane_off = (uint32_t)((tid & 15) * 8);
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {   // chunk = two centroids = 8 dims
-                const uint32_t w = cw[ch >> 1];
-                const int i0 = (ch & 1) * 2;
-                const uint2 e0 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i0 << 4)));
-                const uint2 e1 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)(i0 + 1) << 4)));
-                sts128(sK + sw_off(tid, ch), e0.x, e0.y, e1.x, e1.y);
-            }
-        }
-        // ---- V_hat^T: dims 4vm..4vm+3 of keys j0+vk .. j0+vk+31
-        {
-            uint32_t lo_w[32], hi_w[32];   // dims (0,1) and (2,3) per key
-            const uint32_t lane_off = 128u + (uint32_t)((tid & 15) * 8);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int j = min(j0 + vk + k, a.S_kv - 1);
-                const uint32_t code = vcodes[(int64_t)j * 32 + vm];
-                const uint2 e = lds64(sTab + (code << 8) + lane_off);
-                lo_w[k] = e.x;
-                hi_w[k] = e.y;
-            }
-            // rows 4vm + i, keys vk + 8q .. vk + 8q + 7 -> chunk (vk / 8 + q)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r0[4], r1[4], r2[4], r3[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int k = 8 * q + 2 * p;
-                    r0[p] = __byte_perm(lo_w[k], lo_w[k + 1], 0x5410);
-                    r1[p] = __byte_perm(lo_w[k], lo_w[k + 1], 0x7632);
-                    r2[p] = __byte_perm(hi_w[k], hi_w[k + 1], 0x5410);
-                    r3[p] = __byte_perm(hi_w[k], hi_w[k + 1], 0x7632);
-                }
-                const int ch = vk / 8 + q;
-                sts128(sV + sw_off(4 * vm + 0, ch), r0[0], r0[1], r0[2], r0[3]);
-                sts128(sV + sw_off(4 * vm + 1, ch), r1[0], r1[1], r1[2], r1[3]);
-                sts128(sV + sw_off(4 * vm + 2, ch), r2[0], r2[1], r2[2], r2[3]);
-                sts128(sV + sw_off(4 * vm + 3, ch), r3[0], r3[1], r3[2], r3[3]);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
+        const uint32_t sVj = sV + (uint32_t)(tile & 1) * kTileBytes;
         // ---- S = Q~ K~^T into tensor memory
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
                 const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
-                mma_f16(tmem, smem_desc(sQ + off), smem_desc(sK + off), ks > 0);
+                mma_f16(tmem, smem_desc(sQ + off), smem_desc(sK + off), kIdesc, ks > 0);
             }
             mma_commit(bar_s);
         }
-        // every thread waits (bounded); the verdict is made uniform so that
-        // no thread can leave the loop while others sit in a barrier
-        if (__syncthreads_or(!mbar_wait(bar_s, ph_s))) { failed = true; break; }
+        if (tile < t_last) load_codes(j0 + kKeys);
+        // one thread polls (bounded); the block-wide verdict keeps every
+        // thread on the same path
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(bar_s, ph_s);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_s ^= 1;
         tc_fence_after();
 
-        // ---- online softmax of row `tid` over this tile
+        // ---- online softmax of row `tid` over this tile (masks only where
+        //      some row of the CTA does not see the whole tile)
         const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
         float mx = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
-            float s[32];
-            tmem_ld32(t_s + c * 32, s);
+            for (int c = 0; c < kKeys / 32; ++c) {
+                float sv[32];
+                tmem_ld32(t_s + c * 32, sv);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int j = j0 + c * 32 + i;
-                const float v = (full || (j >= lo && j <= hi)) ? s[i] : -INFINITY;
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < kKeys / 32; ++c) {
+                float sv[32];
+                tmem_ld32(t_s + c * 32, sv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = j0 + c * 32 + i;
+                    mx = fmaxf(mx, (j >= lo && j <= hi) ? sv[i] : -INFINITY);
+                }
             }
         }
         const float m_new = fmaxf(m, mx);
@@ -385,14 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         float lsum = 0.f;
 #pragma unroll
         for (int c = 0; c < kKeys / 32; ++c) {
-            float s[32];
-            tmem_ld32(t_s + c * 32, s);
+            float sv[32];
+            tmem_ld32(t_s + c * 32, sv);
+            if (!full) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = j0 + c * 32 + i;
+                    sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
+                }
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                const int j = j0 + c * 32 + i;
-                const float p0 = (full || (j >= lo && j <= hi)) ? ex2(s[i] - m_use) : 0.f;
-                const float p1 = (full || (j + 1 >= lo && j + 1 <= hi)) ? ex2(s[i + 1] - m_use) : 0.f;
+                const float p0 = ex2(sv[i] - m_use), p1 = ex2(sv[i + 1] - m_use);
                 lsum += p0 + p1;
                 pk[i / 2] = pack_h2(p0, p1);
             }
@@ -405,17 +438,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- P V_hat into tensor memory
+        // ---- P V_hat into tensor memory, next tile's operands meanwhile
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < kKeys / 16; ++ks) {
+                // A = P (K-major, keys along K); B = V_hat rows (keys) of 16
+                // keys = two 8-row groups per step, MN-major
                 const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
-                mma_f16(tmem + kKeys, smem_desc(sP + off), smem_desc(sV + off), ks > 0);
+                mma_f16(tmem + kKeys, smem_desc(sP + off),
+                        smem_desc_mn(sVj + (uint32_t)ks * 2048u, kHalfTile), kIdescBmn, ks > 0);
             }
             mma_commit(bar_o);
         }
-        if (__syncthreads_or(!mbar_wait(bar_o, ph_o))) { failed = true; break; }
+        if (tile < t_last) {
+            build_k();
+            build_v(sV + (uint32_t)((tile + 1) & 1) * kTileBytes);
+            fence_proxy_async();
+        }
+        ok = true;
+        if (tid == 0) ok = mbar_wait(bar_o, ph_o);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_o ^= 1;
         tc_fence_after();
 #pragma unroll
@@ -426,7 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, pv[i]);
         }
         tc_fence_before();
-        __syncthreads();   // K~, V_hat^T, P and tensor memory are reused next tile
     }
 
     // ---- output row
@@ -444,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             *reinterpret_cast<uint4 *>(op + ch * 8) = v;
         }
     }
-    if (failed) {   // let any MMA still in flight finish before freeing its memory
+    if (failed && tid == 0) {   // let MMAs still in flight finish before freeing
         mbar_wait(bar_s, ph_s);
         mbar_wait(bar_o, ph_o);
     }
@@ -458,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 }
 
 size_t prefill_smem_bytes() {
-    return 4 * (size_t)kTileBytes + kTabBytes + 64 + 1024;   // + alignment slack
+    return 5 * (size_t)kTileBytes + kTabBytes + 64 + 1024;   // + alignment slack
 }
 
 }  // namespace
