@@ -20,7 +20,9 @@
 //      is a broadcast, and one centroid load serves all four.  The
 //      scan screens with f_c = |c|^2 - 2 y.c (one fused multiply-add per
 //      dimension; -2c and |c|^2 are staged once), tracking the best and the
-//      second-best value; strict '<' keeps the lowest index on ties.  If
+//      second-best value with min/max only; the group of 8 candidates where
+//      the best last improved is noted and its index found by recomputing
+//      that group (lowest index on ties).  If
 //      the two are closer than twice a rigorous bound on the fp32 error of
 //      that form, the sub-vector is rescanned with the direct form
 //      sum_t (y_t - c_t)^2, so every decision is the one the direct form
@@ -144,13 +146,55 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
 #pragma unroll
             for (int r = 0; r < kR; ++r) load_sub<SUBD>(y_s + (tid + r * kEncThreads) * SUBD, y[r]);
             // screening in the expanded form f_c = |c|^2 - 2 y.c (one fused
-            // multiply-add per dimension), keeping the best and second best
+            // multiply-add per dimension), keeping the best and second-best
+            // value; the best's index is located afterwards: only the group
+            // of kGroup candidates in which the best last improved is noted
+            // (strict '<', so the earliest group wins ties)
+            constexpr int kGroup = 8;
             float f1[kR], f2[kR];
-            int i1[kR];
+            int grp[kR], i1[kR];
 #pragma unroll
-            for (int r = 0; r < kR; ++r) { f1[r] = INFINITY; f2[r] = INFINITY; i1[r] = 0; }
-#pragma unroll 2
-            for (int c = 0; c < N; ++c) {
+            for (int r = 0; r < kR; ++r) { f1[r] = INFINITY; f2[r] = INFINITY; grp[r] = 0; i1[r] = 0; }
+            const int n_full = N & ~(kGroup - 1);
+            for (int g0 = 0; g0 < n_full; g0 += kGroup) {
+                float fb[kR];
+#pragma unroll
+                for (int r = 0; r < kR; ++r) fb[r] = f1[r];
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k) {
+                    float cv[SUBD];
+                    load_sub<SUBD>(cb_s + (g0 + k) * SUBD, cv);
+                    const float nc = nrm_s[g0 + k];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+                        float f = nc;
+#pragma unroll
+                        for (int t = 0; t < SUBD; ++t) f = fmaf(cv[t], y[r][t], f);
+                        f2[r] = fminf(f2[r], fmaxf(f1[r], f));
+                        f1[r] = fminf(f1[r], f);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kR; ++r) grp[r] = f1[r] < fb[r] ? g0 : grp[r];
+            }
+            // index of the best inside its group: recompute that group (the
+            // same arithmetic, so the best value reappears bit for bit)
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                int found = -1;
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k) {
+                    const int c = grp[r] + k;
+                    if (c >= n_full) break;
+                    float f = nrm_s[c];
+#pragma unroll
+                    for (int t = 0; t < SUBD; ++t) f = fmaf(cb_s[c * SUBD + t], y[r][t], f);
+                    if (found < 0 && f == f1[r]) found = c;
+                }
+                i1[r] = found < 0 ? 0 : found;
+            }
+            // candidates past the last full group (N not a multiple of kGroup)
+            for (int c = n_full; c < N; ++c) {
                 float cv[SUBD];
                 load_sub<SUBD>(cb_s + c * SUBD, cv);
                 const float nc = nrm_s[c];
@@ -162,7 +206,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                     f2[r] = fminf(f2[r], fmaxf(f1[r], f));
                     const bool lt = f < f1[r];
                     i1[r] = lt ? c : i1[r];
-                    f1[r] = fminf(f1[r], f);
+                    f1[r] = lt ? f : f1[r];
                 }
             }
             // When the two best screened values are closer than twice the

@@ -8,8 +8,9 @@
 // the companion kernel described under rabitq_prefill_attend (both products
 // on matrix tiles, keys and values decoded inside the tile loop).
 //
-// One CTA = (batch, query head, tile of 128 query rows); thread i owns query
-// row i, which is also tensor-memory lane i of every accumulator.
+// One CTA = (batch, query head, tile of 128 query rows), 256 threads: query
+// row i (tensor-memory lane i of every accumulator) belongs to threads i and
+// i + 128, which take the two 64-column halves of its scores and output.
 //   * Q~ = Hn (q (.) s_g^-1) * scale * log2(e) is built once per CTA (FWHT in
 //     registers) and stored as the A operand in the canonical K-major,
 //     128-byte-swizzled shared-memory layout (fp16).
@@ -43,7 +44,7 @@ namespace {
 constexpr int kRows = 128;        // query rows per CTA (MMA M)
 constexpr int kKeys = 128;        // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;           // head dimension of this kernel
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;     // two threads per query row (column halves)
 constexpr int kSub = 4;           // sub-vector size of both codebooks
 constexpr uint32_t kTileBytes = kRows * kD * 2;  // one fp16 operand tile, 32 KiB
 constexpr uint32_t kHalfTile = kTileBytes / 2;   // 64-element K half, 16 KiB
@@ -202,13 +203,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     unsigned char *tab = gbase + 5 * kTileBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 5 * kTileBytes + kTabBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    float *red = reinterpret_cast<float *>(bars + 4);   // [2][kRows] row exchange
     const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
 
+    // thread = (row r of the tile, column half hh); warps w and w + 4 share
+    // the tensor-memory lanes of rows 32 (w mod 4) ..
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int r = tid & (kRows - 1), hh = tid >> 7;
     const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
     const int g = hq / a.G;
     const int q0 = qt * kRows;
-    const int row = q0 + tid;              // this thread's query row
+    const int row = q0 + r;                // this thread's query row
     const bool row_ok = row < a.S_q;
 
     // ---- tensor memory: S in columns [0, 128), P V_hat in [128, 256)
@@ -239,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             c < n ? pack_h2(cb[c * kSub + t], cb[c * kSub + t + 1]) : 0u;
     }
 
-    // ---- Q~ row of this thread (fp16, swizzled A operand)
-    {
+    // ---- Q~ row r (fp16, swizzled A operand), by the first column half
+    if (hh == 0) {
         float x[kD];
         if (row_ok) {
             const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 #pragma unroll
         for (int ch = 0; ch < kD / 8; ++ch) {
             const float *p = x + ch * 8;
-            sts128(sQ + sw_off(tid, ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
+            sts128(sQ + sw_off(r, ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
                    pack_h2(p[2] * a.qscale, p[3] * a.qscale),
                    pack_h2(p[4] * a.qscale, p[5] * a.qscale),
                    pack_h2(p[6] * a.qscale, p[7] * a.qscale));
@@ -299,44 +304,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     const int all_hi = min(a.causal ? qa_first : a.S_kv - 1, a.S_kv - 1);
     const int t_first = cta_lo / kKeys, t_last = cta_hi / kKeys;
 
-    float o[kD];
+    constexpr int kHalfD = kD / 2, kHalfKeys = kKeys / 2;
+    float o[kHalfD];                       // output dims hh*64 .. hh*64+63
 #pragma unroll
-    for (int e = 0; e < kD; ++e) o[e] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    for (int e = 0; e < kHalfD; ++e) o[e] = 0.f;
+    float m = -INFINITY, l = 0.f;          // l: this half's share of the row sum
     uint32_t ph_s = 0, ph_o = 0;
     bool failed = false;
 
     const int64_t bg = (int64_t)b * a.H_kv + g;
-    const uint8_t *kcodes = a.kc + bg * a.S_kv * 32;
-    const uint8_t *vcodes = a.vc + bg * a.S_kv * 32;
+    const uint8_t *kcodes = a.kc + bg * a.S_kv * 32 + hh * 16;
+    const uint8_t *vcodes = a.vc + bg * a.S_kv * 32 + hh * 16;
 
-    // codes of one tile in registers: key row `tid`, K and V side
-    uint32_t kcw[8], vcw[8];
+    // codes of one tile in registers: the 16 codes (dims hh*64 ..) of the
+    // tile's key r, K and V side
+    uint32_t kcw[4], vcw[4];
     auto load_codes = [&](int j0) {
-        const int j = min(j0 + tid, a.S_kv - 1);
+        const int j = min(j0 + r, a.S_kv - 1);
         const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
         const uint4 d0 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32);
-        const uint4 d1 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32 + 16);
         kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
-        kcw[4] = c1.x; kcw[5] = c1.y; kcw[6] = c1.z; kcw[7] = c1.w;
         vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
-        vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
     };
-    // Row `tid` (the tile's key `tid`) of a [keys x D] fp16 tile: 32
+    // Half hh of row r (the tile's key r) of a [keys x D] fp16 tile: 16
     // centroids, two per 16-byte chunk, 128-byte swizzle.  The same image
     // serves as K~ (B of Q~K~^T, K-major) and as V_hat (B of P V_hat, read
     // MN-major: keys along K, dims contiguous).
     auto build_rows = [&](const uint32_t *cw, uint32_t dst, uint32_t half_off) {
         const uint32_t lane_off = half_off + (uint32_t)((tid & 15) * 8);
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-            const uint32_t w = cw[ch >> 1];
-            const int i0 = (ch & 1) * 2;
+        for (int cc = 0; cc < 8; ++cc) {
+            const uint32_t w = cw[cc >> 1];
+            const int i0 = (cc & 1) * 2;
             const uint2 e0 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i0 << 4)));
             const uint2 e1 =
                 lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)(i0 + 1) << 4)));
-            sts128(dst + sw_off(tid, ch), e0.x, e0.y, e1.x, e1.y);
+            sts128(dst + sw_off(r, hh * 8 + cc), e0.x, e0.y, e1.x, e1.y);
         }
     };
     auto build_k = [&]() { build_rows(kcw, sK, 0u); };
@@ -357,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t t_o = t_s + kKeys;
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lanes + (uint32_t)(hh * kHalfKeys);
+    const uint32_t t_o = tmem + lanes + (uint32_t)(kKeys + hh * kHalfD);
 
     for (int tile = t_first; tile <= t_last; ++tile) {
         const int j0 = tile * kKeys;
@@ -382,43 +386,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         ph_s ^= 1;
         tc_fence_after();
 
-        // ---- online softmax of row `tid` over this tile (masks only where
-        //      some row of the CTA does not see the whole tile)
+        // ---- online softmax of row r over this tile: each half takes 64
+        //      keys; the halves exchange their maxima through shared memory
         const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
+        const int jh = j0 + hh * kHalfKeys;
         float mx = -INFINITY;
-        if (full) {
 #pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float sv[32];
-                tmem_ld32(t_s + c * 32, sv);
+        for (int c = 0; c < kHalfKeys / 32; ++c) {
+            float sv[32];
+            tmem_ld32(t_s + c * 32, sv);
+            if (full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float sv[32];
-                tmem_ld32(t_s + c * 32, sv);
+            } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int j = j0 + c * 32 + i;
+                    const int j = jh + c * 32 + i;
                     mx = fmaxf(mx, (j >= lo && j <= hi) ? sv[i] : -INFINITY);
                 }
             }
         }
+        red[hh * kRows + r] = mx;
+        __syncthreads();
+        mx = fmaxf(red[r], red[kRows + r]);
         const float m_new = fmaxf(m, mx);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2(m - m_use);
         m = m_new;
         float lsum = 0.f;
 #pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
+        for (int c = 0; c < kHalfKeys / 32; ++c) {
             float sv[32];
             tmem_ld32(t_s + c * 32, sv);
             if (!full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int j = j0 + c * 32 + i;
+                    const int j = jh + c * 32 + i;
                     sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
                 }
             }
@@ -431,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                sts128(sP + sw_off(tid, c * 4 + q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                       pk[4 * q + 3]);
+                sts128(sP + sw_off(r, hh * 8 + c * 4 + q), pk[4 * q], pk[4 * q + 1],
+                       pk[4 * q + 2], pk[4 * q + 3]);
         }
         l = l * alpha + lsum;
         fence_proxy_async();
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         ph_o ^= 1;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
             float pv[32];
             tmem_ld32(t_o + c * 32, pv);
 #pragma unroll
@@ -471,12 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         tc_fence_before();
     }
 
-    // ---- output row
+    // ---- output row: the two halves' sums combine into the row's l
+    __syncthreads();
+    red[hh * kRows + r] = l;
+    __syncthreads();
+    l = red[r] + red[kRows + r];
     if (row_ok) {
-        __half *op = a.out + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD;
+        __half *op = a.out + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD + hh * kHalfD;
         const float inv = failed ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
 #pragma unroll
-        for (int ch = 0; ch < kD / 8; ++ch) {
+        for (int ch = 0; ch < kHalfD / 8; ++ch) {
             const float *p = o + ch * 8;
             uint4 v;
             v.x = pack_h2(p[0] * inv, p[1] * inv);
@@ -500,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 }
 
 size_t prefill_smem_bytes() {
-    return 5 * (size_t)kTileBytes + kTabBytes + 64 + 1024;   // + alignment slack
+    return 5 * (size_t)kTileBytes + kTabBytes + 32 + 2 * kRows * sizeof(float) +
+           1024;   // + alignment slack
 }
 
 }  // namespace
