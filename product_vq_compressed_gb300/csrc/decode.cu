@@ -150,30 +150,30 @@ __device__ __forceinline__ void gather(uint32_t addr, uint32_t *w) {
 }
 
 // Fast-path gathers: uint8 codes and one interleaved table of 256 rows x 256
-// bytes at shared-memory offset 0 -- row c holds the key centroid c replicas
-// in bytes [0, 128) and the value centroid c replicas in [128, 256).  The
-// address of the row for code byte i of word w plus the lane's replica
-// offset (< 256) is then a single byte permute: bytes (off, code, 0, 0).
+// bytes placed at shared-memory address 65536 -- row c holds the key
+// centroid c replicas in bytes [0, 128) and the value centroid c replicas in
+// [128, 256).  The shared address of the row for code byte i of word w plus
+// the lane's replica offset (< 256) is then a single byte permute:
+// bytes (off, code, 1, 0) = 65536 + code * 256 + off.
 // i is a constant once the caller's loop is unrolled.
+constexpr uint32_t kFastTabAddr = 65536;
 __device__ __forceinline__ uint32_t row_off(uint32_t w, int i, uint32_t lane_off) {
-    return __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i << 4));
+    return __byte_perm(w, lane_off | (1u << 16), 0x7604u | ((uint32_t)i << 4));
 }
 
 template <int SUB>
-__device__ __forceinline__ void gather_at(const unsigned char *p, uint32_t *w) {
+__device__ __forceinline__ void gather_sh(uint32_t addr, uint32_t *w) {
     if constexpr (SUB == 2) {
-        w[0] = *reinterpret_cast<const uint32_t *>(p);
+        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(w[0]) : "r"(addr));
     } else if constexpr (SUB == 4) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
-        w[0] = v.x; w[1] = v.y;
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
     } else {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p);
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
     }
 }
 
 constexpr uint32_t kFastRow = 256;                 // bytes per interleaved row
-constexpr uint32_t kFastTable = 256 * kFastRow;    // 64 KiB
 
 __host__ __device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
@@ -243,22 +243,31 @@ struct StepCodes {
 __device__ __forceinline__ int krow_of(int g8, int r) { return g8 + 8 * r; }
 __device__ __forceinline__ int vrow_of(int c4, int r) { return 2 * c4 + (r & 1) + 8 * (r >> 1); }
 
-template <int D, int DK, int DV>
+template <int D, int DK, int DV, bool FAST>
 __device__ __forceinline__ void load_step(StepCodes<D, DK, DV> &sc, const uint8_t *kl,
                                           const uint8_t *vl, int j0, const DecArgs &a,
-                                          int64_t ktb, int64_t vtb, int g8, int c4) {
+                                          int64_t ktb_rt, int64_t vtb_rt, int g8, int c4) {
     using SC = StepCodes<D, DK, DV>;
+    // uint8 codes on the fast path: strides are compile-time constants
+    const int64_t ktb = FAST ? (int64_t)(D / DK) : ktb_rt;
+    const int64_t vtb = FAST ? (int64_t)(D / DV) : vtb_rt;
+    auto ld_k = [&](const uint8_t *p, uint32_t *w) {
+        if constexpr (FAST) load_bytes<SC::NKL>(p, w);
+        else load_codes<SC::NKL>(p, a.kcb, w);
+    };
+    auto ld_v = [&](const uint8_t *p, uint32_t *w) {
+        if constexpr (FAST) load_bytes<SC::NVL>(p, w);
+        else load_codes<SC::NVL>(p, a.vcb, w);
+    };
     if (j0 + kStepKeys <= a.S_kv) {
 #pragma unroll
         for (int t = 0; t < kStepTiles; ++t) {
 #pragma unroll
             for (int r = 0; r < 2; ++r)
-                load_codes<SC::NKL>(kl + (int64_t)(j0 + t * kTile + 8 * r) * ktb, a.kcb,
-                                    sc.k[t][r]);
+                ld_k(kl + (int64_t)(j0 + t * kTile + 8 * r) * ktb, sc.k[t][r]);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                load_codes<SC::NVL>(vl + (int64_t)(j0 + t * kTile + (r & 1) + 8 * (r >> 1)) * vtb,
-                                    a.vcb, sc.v[t][r]);
+                ld_v(vl + (int64_t)(j0 + t * kTile + (r & 1) + 8 * (r >> 1)) * vtb, sc.v[t][r]);
         }
     } else {  // tail of the cache: clamp rows past the last key (masked later)
 #pragma unroll
@@ -266,12 +275,12 @@ __device__ __forceinline__ void load_step(StepCodes<D, DK, DV> &sc, const uint8_
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int j = min(j0 + t * kTile + krow_of(g8, r), a.S_kv - 1) - krow_of(g8, 0);
-                load_codes<SC::NKL>(kl + (int64_t)j * ktb, a.kcb, sc.k[t][r]);
+                ld_k(kl + (int64_t)j * ktb, sc.k[t][r]);
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int j = min(j0 + t * kTile + vrow_of(c4, r), a.S_kv - 1) - vrow_of(c4, 0);
-                load_codes<SC::NVL>(vl + (int64_t)j * vtb, a.vcb, sc.v[t][r]);
+                ld_v(vl + (int64_t)j * vtb, sc.v[t][r]);
             }
         }
     }
@@ -301,7 +310,7 @@ __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const 
                                             const unsigned char *tab, uint32_t lane_off,
                                             uint32_t *w) {
     if constexpr (FAST) {
-        gather_at<DKV>(tab + row_off(words[u >> 2], u & 3, lane_off), w);
+        gather_sh<DKV>(row_off(words[u >> 2], u & 3, lane_off), w);
     } else {
         const uint32_t code = min(code_at<NC>(words, cb, u), (uint32_t)(N - 1));
         gather<DKV>(base + code * (uint32_t)row, w);
@@ -443,12 +452,17 @@ decode_kernel(DecArgs a) {
     //   otherwise: key table (N_k rows) then value table (N_v rows)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int krow = a.k_copies * EK, vrow = a.v_copies * EV;   // replica bytes per row
-    unsigned char *ktab = smem_raw;
-    unsigned char *vtab = FAST ? smem_raw + 128 : smem_raw + align16((size_t)a.Nk * krow);
-    const size_t tab_bytes = FAST ? (size_t)kFastTable
+    const size_t tab_bytes = FAST ? (size_t)0
                                   : align16((size_t)a.Nk * krow) + align16((size_t)a.Nv * vrow);
+    // fast path: scratch and staging first, the table at shared address
+    // 65536 (the launch reserves 128 KiB, which always reaches past it)
+    unsigned char *ktab = FAST ? smem_raw + (kFastTabAddr - (uint32_t)__cvta_generic_to_shared(smem_raw))
+                               : smem_raw;
+    unsigned char *vtab = FAST ? ktab + 128 : smem_raw + align16((size_t)a.Nk * krow);
     WarpScratch<D> *scratch = reinterpret_cast<WarpScratch<D> *>(smem_raw + tab_bytes);
     float *stage = reinterpret_cast<float *>(scratch + kWarps);
+    if (FAST && (uint32_t)__cvta_generic_to_shared(stage + a.Nk * DK + a.Nv * DV) > kFastTabAddr)
+        return;   // not reachable: dynamic shared memory starts near address 0
     const int kstride = FAST ? (int)kFastRow : krow;   // row strides of the tables
     const int vstride = FAST ? (int)kFastRow : vrow;
     const int nk_rows = FAST ? 256 : a.Nk, nv_rows = FAST ? 256 : a.Nv;
@@ -590,17 +604,17 @@ decode_kernel(DecArgs a) {
         us.lo_all = max(us.lo_all, j_first); us.hi_all = min(us.hi_all, j_last - 1);
         SC ca, cb;
         int j = j_first;
-        load_step<D, DK, DV>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
+        load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
         while (j < j_last) {
             if (j + kStepKeys < j_last)
-                load_step<D, DK, DV>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+                load_step<D, DK, DV, FAST>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
             prefetch(j + kPrefetchTiles * kTile);
             process_step<D, DK, DV, FAST>(ca, j, us, a, kbase, vbase, krow, vrow, g8, c4,
                                           smem_raw, klane, vlane);
             j += kStepKeys;
             if (j >= j_last) break;
             if (j + kStepKeys < j_last)
-                load_step<D, DK, DV>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+                load_step<D, DK, DV, FAST>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
             prefetch(j + kPrefetchTiles * kTile);
             process_step<D, DK, DV, FAST>(cb, j, us, a, kbase, vbase, krow, vrow, g8, c4,
                                           smem_raw, klane, vlane);
@@ -700,9 +714,11 @@ Tables choose_tables(const vq_attend_args &a) {
     const size_t tail = scratch_bytes(a.D) +
                         sizeof(float) * ((size_t)a.k_n_centroids * a.k_sub_dim +
                                          (size_t)a.v_n_centroids * a.v_sub_dim);
+    // fast path: the table sits at shared address 64 KiB, scratch and
+    // staging below it (dynamic shared memory starts within the first KiB)
     if (a.k_code_bytes == 1 && a.v_code_bytes == 1 && a.k_n_centroids <= 256 &&
-        a.v_n_centroids <= 256 && (size_t)kFastTable + tail <= kSmemBudget)
-        return {128 / ek, 128 / ev, true, (size_t)kFastTable + tail};
+        a.v_n_centroids <= 256 && tail + 2048 <= kFastTabAddr)
+        return {128 / ek, 128 / ev, true, 2 * (size_t)kFastTabAddr};
     int kc = 128 / ek, vc = 128 / ev;
     auto total = [&](int k, int v) {
         return align16((size_t)a.k_n_centroids * k * ek) +

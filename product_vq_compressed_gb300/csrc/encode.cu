@@ -161,17 +161,24 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
 #pragma unroll
                 for (int r = 0; r < kR; ++r) fb[r] = f1[r];
 #pragma unroll
-                for (int k = 0; k < kGroup; ++k) {
-                    float cv[SUBD];
-                    load_sub<SUBD>(cb_s + (g0 + k) * SUBD, cv);
-                    const float nc = nrm_s[g0 + k];
+                for (int k = 0; k < kGroup; k += 2) {   // two candidates per round
+                    float ca[SUBD], cb[SUBD];
+                    load_sub<SUBD>(cb_s + (g0 + k) * SUBD, ca);
+                    load_sub<SUBD>(cb_s + (g0 + k + 1) * SUBD, cb);
+                    const float na = nrm_s[g0 + k], nb = nrm_s[g0 + k + 1];
 #pragma unroll
                     for (int r = 0; r < kR; ++r) {
-                        float f = nc;
+                        float fa = na, fb = nb;
 #pragma unroll
-                        for (int t = 0; t < SUBD; ++t) f = fmaf(cv[t], y[r][t], f);
-                        f2[r] = fminf(f2[r], fmaxf(f1[r], f));
-                        f1[r] = fminf(f1[r], f);
+                        for (int t = 0; t < SUBD; ++t) {
+                            fa = fmaf(ca[t], y[r][t], fa);
+                            fb = fmaf(cb[t], y[r][t], fb);
+                        }
+                        // second smallest of {f1 <= f2, fa, fb}:
+                        // min(f2, max(f1, min(fa, fb)), max(fa, fb))
+                        const float lo = fminf(fa, fb), hi = fmaxf(fa, fb);
+                        f2[r] = fminf(fminf(f2[r], fmaxf(f1[r], lo)), hi);
+                        f1[r] = fminf(f1[r], lo);
                     }
                 }
 #pragma unroll
