@@ -93,6 +93,25 @@ def peak_for(bound, peaks):
     return 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, "TFLOP/s"
 
 
+# ------------------------------------------------------------- ranks
+
+def max_over_ranks(seconds: float, world: int, device: str) -> float:
+    """Slowest rank's timed seconds (all ranks join; identity at world 1)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Weak scaling: every rank runs its own replica of the workload, so the
+    job processes units_per_rank * world units in the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
 # ------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -242,7 +261,10 @@ def run_gpu(args, name, rank, world):
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for k in range(K):
-            flush.fill_(float(k))            # evict L2 between timed steps
+            # evict L2 between timed steps: the flush starts after the
+            # previous step and the next step after the flush
+            torch.cuda.current_stream().wait_stream(stream)
+            flush.fill_(float(k))
             stream.wait_stream(torch.cuda.current_stream())
             e_start, e_mid, e_end = evs[k]
             launches += r.step(ev=(e_start, e_mid))
@@ -257,13 +279,8 @@ def run_gpu(args, name, rank, world):
         print("warning: non-finite values in the step's output", file=sys.stderr)
     step_ms = [evs[k][0].elapsed_time(evs[k][2]) for k in range(K)]
     dom_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(K)]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    units = units_per_step(name, spec) * K * world
-    value = units / total_s
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, "cuda")
+    value = whole_job_value(units_per_step(name, spec) * K, world, total_s)
 
     # ---- end to end from pinned host buffers (same C-ABI calls)
     e2e = None

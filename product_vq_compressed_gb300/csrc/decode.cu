@@ -199,15 +199,18 @@ struct DecArgs {
     int n_colblk;
     int tlo, T;        // every unit scans key tiles [tlo, tlo + T)
     int64_t total;     // units * T, the flattened work
+    int64_t share;     // tiles per warp (the last shares may be shorter or empty)
     int nw;            // warps sharing the work
     int slots;         // partial records per warp
     int k_copies, v_copies;
 };
 
-// Start of warp gw's contiguous share of the flattened (unit, tile) space.
-__host__ __device__ __forceinline__ int64_t share_start(int64_t gw, int64_t total,
-                                                         int64_t nw) {
-    return gw * total / nw;
+// Warp gw's contiguous share of the flattened (unit, tile) space is
+// [gw * share, min((gw + 1) * share, total)).
+__host__ __device__ __forceinline__ int64_t share_start(int64_t gw, int64_t share,
+                                                         int64_t total) {
+    const int64_t s = gw * share;
+    return s < total ? s : total;
 }
 
 template <int D>
@@ -500,8 +503,8 @@ decode_kernel(DecArgs a) {
 
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
     if (gw >= a.nw) return;
-    int64_t t = share_start(gw, a.total, a.nw);
-    const int64_t t_end = share_start(gw + 1, a.total, a.nw);
+    int64_t t = share_start(gw, a.share, a.total);
+    const int64_t t_end = share_start(gw + 1, a.share, a.total);
     int slot = 0;
     while (t < t_end) {
         const int64_t unit = t / a.T;
@@ -647,10 +650,14 @@ decode_kernel(DecArgs a) {
     }
 }
 
-// Merge the partial records of every (unit, column) and write fp16.
+// Merge the partial records of every (unit, column) and write fp16.  The
+// records of a unit come from the warps whose shares overlap it; the block
+// reduces their maxima and sums in parallel, then every thread (one output
+// dimension) accumulates the rescaled partial outputs.
 template <int D>
 __global__ void __launch_bounds__(D)
 combine_kernel(DecArgs a, __half *__restrict__ out) {
+    __shared__ float red[D / 32];
     const int64_t unit = blockIdx.x;
     const int col = blockIdx.y;
     const int cblk = (int)(unit % a.n_colblk);
@@ -659,29 +666,47 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
     if (cg >= a.G * a.S_q) return;
     const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
     const int i = cg / a.G, gam = cg % a.G;
-    const int d = threadIdx.x;
-    const int64_t u0 = unit * a.T, u1 = u0 + a.T;
-    // first warp whose share ends after u0
-    int64_t gw = u0 * a.nw / (a.total > 0 ? a.total : 1);
-    gw = gw > 0 ? gw - 1 : 0;
-    while (gw < a.nw && share_start(gw + 1, a.total, a.nw) <= u0) ++gw;
+    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int64_t u0 = unit * a.T;
+    const int64_t w_lo = u0 / a.share;
+    int64_t w_hi = (u0 + a.T - 1) / a.share;
+    if (w_hi > a.nw - 1) w_hi = a.nw - 1;
+    const int n_rec = (int)(w_hi - w_lo + 1);
+    // record of warp w for this unit: slot = unit - (first unit of w)
+    auto rec_of = [&](int k) -> const float * {
+        const int64_t w = w_lo + k;
+        const int64_t s = w * a.share;
+        const int64_t slot = a.share <= a.T ? (s >= u0 ? 0 : 1) : unit - s / a.T;
+        return a.ws + ((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4);
+    };
+    auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, off);
+            v = is_max ? fmaxf(v, o) : v + o;
+        }
+        __syncthreads();
+        if (lane == 0) red[warp] = v;
+        __syncthreads();
+        v = red[0];
+        for (int w = 1; w < D / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+        return v;
+    };
     float M = -INFINITY;
-    for (int64_t w = gw; w < a.nw && share_start(w, a.total, a.nw) < u1; ++w) {
-        const int64_t s = share_start(w, a.total, a.nw);
-        if (share_start(w + 1, a.total, a.nw) == s) continue;
-        const int64_t slot = unit - s / a.T;
-        M = fmaxf(M, a.ws[((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4)]);
-    }
-    float o = 0.f, l = 0.f;
+    for (int k = d; k < n_rec; k += D) M = fmaxf(M, rec_of(k)[0]);
+    M = block_reduce(M, true);
+    float o = 0.f;
     if (M != -INFINITY) {
-        for (int64_t w = gw; w < a.nw && share_start(w, a.total, a.nw) < u1; ++w) {
-            const int64_t s = share_start(w, a.total, a.nw);
-            if (share_start(w + 1, a.total, a.nw) == s) continue;
-            const int64_t slot = unit - s / a.T;
-            const float *rec = a.ws + ((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4);
-            const float f = exp2f(rec[0] - M);
-            l += f * rec[1];
-            o += f * rec[4 + d];
+        float l = 0.f;
+        for (int k = d; k < n_rec; k += D) {
+            const float *r = rec_of(k);
+            l += exp2f(r[0] - M) * r[1];
+        }
+        l = block_reduce(l, false);
+#pragma unroll 4
+        for (int k = 0; k < n_rec; ++k) {
+            const float *r = rec_of(k);
+            o += exp2f(r[0] - M) * r[4 + d];
         }
         o = l > 0.f ? o / l : 0.f;
     }
@@ -781,7 +806,7 @@ void tile_range(const vq_attend_args &a, int *tlo, int *T) {
     *T = hi / kTile - *tlo + 1;
 }
 
-constexpr int kMinTilesPerWarp = 8;
+constexpr int kMinTilesPerWarp = 4;
 
 }  // namespace
 
@@ -814,9 +839,11 @@ AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
     const int64_t by_size = (p.total + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
     if (nw > by_size) nw = by_size;
     if (nw < 1) nw = 1;
-    p.n_warps = nw;
-    p.grid = (int)((nw + kWarps - 1) / kWarps);
     const int64_t share = (p.total + nw - 1) / nw;
+    nw = (p.total + share - 1) / share;   // drop warps left without work
+    p.n_warps = nw;
+    p.share = share;
+    p.grid = (int)((nw + kWarps - 1) / kWarps);
     p.slots = (int)((share + T - 1) / T + 1);
     p.n_split = 1;
     p.tok_per_split = T * kTile;
@@ -833,9 +860,11 @@ AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms, size_t max_w
     while (nw > 1) {
         nw = nw / 2;
         const int64_t share = (p.total + nw - 1) / nw;
+        nw = (p.total + share - 1) / share;
         const int slots = (int)((share + p.tiles - 1) / p.tiles + 1);
         if ((size_t)nw * slots * rec <= max_ws_bytes) {
             p.n_warps = nw;
+            p.share = share;
             p.grid = (int)((nw + warps_for(a.D) - 1) / warps_for(a.D));
             p.slots = slots;
             p.ws_bytes = (size_t)nw * slots * rec;
@@ -874,6 +903,7 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.tlo = plan.tile_lo;
     da.T = plan.tiles;
     da.total = plan.total;
+    da.share = plan.share;
     da.nw = (int)plan.n_warps;
     da.slots = plan.slots;
     da.k_copies = tb.k_copies;

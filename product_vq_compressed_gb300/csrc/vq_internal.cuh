@@ -50,6 +50,7 @@ struct AttendPlan {
     int tile_lo, tiles; // every unit scans key tiles [tile_lo, tile_lo + tiles)
     int64_t total;      // units * tiles
     int64_t n_warps;    // warps sharing the flattened work
+    int64_t share;      // tiles per warp (contiguous shares)
     int grid;           // CTAs
     int slots;          // partial records per warp
     size_t ws_bytes;    // partial records
