@@ -651,13 +651,21 @@ decode_kernel(DecArgs a) {
 }
 
 // Merge the partial records of every (unit, column) and write fp16.  The
-// records of a unit come from the warps whose shares overlap it; the block
-// reduces their maxima and sums in parallel, then every thread (one output
-// dimension) accumulates the rescaled partial outputs.
+// records of a unit come from the warps whose shares overlap it.  The block
+// (256 threads) reduces their maxima and sums in parallel and keeps each
+// record's rescale factor in shared memory; then 256 / D groups of D threads
+// (one output dimension each) accumulate disjoint subsets of the records with
+// many loads in flight, and the groups' sums are added.
+constexpr int kCombThreads = 256;
+constexpr int kMaxRecords = 2048;   // >= warps of any plan (one CTA per SM)
+
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kCombThreads)
 combine_kernel(DecArgs a, __half *__restrict__ out) {
-    __shared__ float red[D / 32];
+    constexpr int kGroups = kCombThreads / D;
+    __shared__ float fac[kMaxRecords];
+    __shared__ float red[kCombThreads / 32];
+    __shared__ float part[kGroups][D];
     const int64_t unit = blockIdx.x;
     const int col = blockIdx.y;
     const int cblk = (int)(unit % a.n_colblk);
@@ -666,12 +674,14 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
     if (cg >= a.G * a.S_q) return;
     const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
     const int i = cg / a.G, gam = cg % a.G;
-    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = tid % D, grp = tid / D;
     const int64_t u0 = unit * a.T;
     const int64_t w_lo = u0 / a.share;
     int64_t w_hi = (u0 + a.T - 1) / a.share;
     if (w_hi > a.nw - 1) w_hi = a.nw - 1;
-    const int n_rec = (int)(w_hi - w_lo + 1);
+    int n_rec = (int)(w_hi - w_lo + 1);
+    if (n_rec > kMaxRecords) n_rec = kMaxRecords;   // not reachable: see kMaxRecords
     // record of warp w for this unit: slot = unit - (first unit of w)
     auto rec_of = [&](int k) -> const float * {
         const int64_t w = w_lo + k;
@@ -689,29 +699,39 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
         if (lane == 0) red[warp] = v;
         __syncthreads();
         v = red[0];
-        for (int w = 1; w < D / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+#pragma unroll
+        for (int w = 1; w < kCombThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
         return v;
     };
     float M = -INFINITY;
-    for (int k = d; k < n_rec; k += D) M = fmaxf(M, rec_of(k)[0]);
+    for (int k = tid; k < n_rec; k += kCombThreads) {
+        const float m = rec_of(k)[0];
+        fac[k] = m;
+        M = fmaxf(M, m);
+    }
     M = block_reduce(M, true);
     float o = 0.f;
     if (M != -INFINITY) {
         float l = 0.f;
-        for (int k = d; k < n_rec; k += D) {
-            const float *r = rec_of(k);
-            l += exp2f(r[0] - M) * r[1];
+        for (int k = tid; k < n_rec; k += kCombThreads) {
+            const float f = exp2f(fac[k] - M);
+            fac[k] = f;
+            l += f * rec_of(k)[1];
         }
-        l = block_reduce(l, false);
-#pragma unroll 4
-        for (int k = 0; k < n_rec; ++k) {
-            const float *r = rec_of(k);
-            o += exp2f(r[0] - M) * r[4 + d];
-        }
+        l = block_reduce(l, false);   // its barriers also publish fac[]
+#pragma unroll 8
+        for (int k = grp; k < n_rec; k += kGroups) o += fac[k] * rec_of(k)[4 + d];
+        part[grp][d] = o;
+        __syncthreads();
+        o = 0.f;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) o += part[q][d];
         o = l > 0.f ? o / l : 0.f;
     }
-    const int hq = g * a.G + gam;
-    out[(((int64_t)b * a.H_q + hq) * a.S_q + i) * D + d] = __float2half_rn(o);
+    if (grp == 0) {
+        const int hq = g * a.G + gam;
+        out[(((int64_t)b * a.H_q + hq) * a.S_q + i) * D + d] = __float2half_rn(o);
+    }
 }
 
 struct Tables {
@@ -838,6 +858,7 @@ AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
     int64_t nw = (int64_t)num_sms * kWarps;
     const int64_t by_size = (p.total + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
     if (nw > by_size) nw = by_size;
+    if (nw > kMaxRecords) nw = kMaxRecords;   // the combine holds one factor per warp
     if (nw < 1) nw = 1;
     const int64_t share = (p.total + nw - 1) / nw;
     nw = (p.total + share - 1) / share;   // drop warps left without work
@@ -921,10 +942,10 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     dim3 cgrid((unsigned)units, kCols);
     __half *out = reinterpret_cast<__half *>(a.out_f16);
     switch (a.D) {
-        case 32: combine_kernel<32><<<cgrid, 32, 0, stream>>>(da, out); break;
-        case 64: combine_kernel<64><<<cgrid, 64, 0, stream>>>(da, out); break;
-        case 128: combine_kernel<128><<<cgrid, 128, 0, stream>>>(da, out); break;
-        default: combine_kernel<256><<<cgrid, 256, 0, stream>>>(da, out); break;
+        case 32: combine_kernel<32><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
+        case 64: combine_kernel<64><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
+        case 128: combine_kernel<128><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
+        default: combine_kernel<256><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
     }
     return cudaGetLastError();
 }

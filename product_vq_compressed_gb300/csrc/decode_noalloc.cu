@@ -31,7 +31,7 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = VQ_NOALLOC_SCRATCH_BYTES;
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
