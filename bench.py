@@ -93,6 +93,21 @@ def peak_for(bound, peaks):
     return 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, "TFLOP/s"
 
 
+def measured_traffic(name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        entry = json.load(open(path))[name]
+        src = open(os.path.join(ROOT, entry["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha256(src).hexdigest() != entry["sha256"]:
+        return None
+    return entry["bytes_per_launch"]
+
+
 # ------------------------------------------------------------- ranks
 
 def max_over_ranks(seconds: float, world: int, device: str) -> float:
@@ -323,7 +338,7 @@ def run_gpu(args, name, rank, world):
     achieved = (work / dom_s) / (1e9 if wunit == "GB/s" else 1e12)
     roof = {"bound": bound, "kernel": kernel, "achieved": round(achieved, 3),
             "peak": round(peak, 1), "unit": punit, "frac": round(achieved / peak, 4),
-            "peak_source": peak_src, "traffic": None,
+            "peak_source": peak_src, "traffic": measured_traffic(name),
             "kernel_ms": round(dom_s * 1e3, 4)}
     clocks = clk.summary()
     metric, unit = METRICS[name]
