@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libvqkv.so")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
-SOURCES = ["vqkv_api.cu", "encode.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu"]
+SOURCES = ["vqkv_api.cu", "encode.cu", "encode_mma.cu", "decode.cu", "prefill.cu",
+           "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

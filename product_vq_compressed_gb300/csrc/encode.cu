@@ -352,6 +352,7 @@ size_t encode_smem_bytes(int N, int sub_dim) {
 }
 
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream) {
+    if (encode_mma_supported(p.N, p.sub_dim)) return launch_encode_mma(p, stream);
     switch (p.sub_dim) {
         case 1: return launch_encode_c<1>(p, stream);
         case 2: return launch_encode_c<2>(p, stream);

@@ -1,0 +1,627 @@
+// encode_mma.cu -- key / value encode with the candidate screening on the
+// tensor cores (warp-level mma.sync m16n8k16, fp16 operands, fp32 sums).
+//
+// Same operation as encode.cu (page "Metal Kernels API", section "VecInfer
+// kernels": vecinfer_encode_decode_metal, its value-side sibling and
+// vecinfer_quantize_metal): y = Hn (s (.) x), code = nearest centroid of
+// every sub-vector by squared distance, lowest index on ties, optional
+// reconstruction.  The rotation and the search are organised differently.
+//
+// Rotation.  One warp per token holds the token in registers (D/32
+// consecutive elements per lane), applies the butterflies below the lane
+// stride locally and the rest with xor-shuffles, in the same stage order as
+// the shared-memory transform of encode.cu, so y is bit-identical.
+//
+// Screening.  For sub-vector y and centroid c, f_c = |c|^2 - 2 y.c orders
+// the candidates like |y - c|^2.  It is one matrix product: rows
+// [y_hi, y_lo, y_hi, 1, 1] times columns [-2c_hi, -2c_hi, -2c_lo, |c|^2_hi,
+// |c|^2_lo], with x_hi = fp16(x) and x_lo = fp16(x - x_hi).  The split keeps
+// about 22 bits of each operand; `screen_bound` is a rigorous bound E on
+// the difference to the exact f_c.
+//
+// Selection.  Per row, the four lanes of a quad see disjoint candidates (two
+// columns of every 8-centroid n-tile).  A lane keeps only the minimum of
+// each block of 64 centroids (its 16 of them, by 3-input min), writes the
+// block and its quad position into the low mantissa bits of that minimum
+// (moving it by less than 2^tbits ulp, accounted for below), and keeps the
+// best and second-best tagged minimum over blocks.  A reduce-scatter over
+// the quad leaves each lane the merged pair of one row.
+//
+// Exact decision.  The lane evaluates the 16 candidates of the winning
+// (block, lane) in fp32 in the direct form sum_t (y_t - c_t)^2, in index
+// order with strict '<' (lowest index on ties).  Every other candidate has
+// exact distance >= (second best, untagged) + |y|^2 - E; unless that bound
+// clears the best direct value by the fp32 error margins, the warp rescans
+// the whole row in the direct form.  So every code is the direct-form fp32
+// argmin wherever that differs from the exact one, as in encode.cu.
+#include <math.h>
+
+#include "vq_internal.cuh"
+
+namespace vqkv {
+namespace {
+
+constexpr int kThr = 256;           // 8 warps
+constexpr int kSlots = 512;         // sub-vectors per tile (64 per warp)
+constexpr int kPassRows = 32;       // rows per warp pass (two 16-row m-tiles)
+constexpr int kBlockCols = 64;      // centroids per screening block (8 n-tiles)
+constexpr float kU = 5.9604645e-8f;    // 2^-24
+constexpr float kU22 = 2.3841858e-7f;  // 2^-22
+constexpr float kBigNorm = 30000.f; // |c|^2 of padding centroids (c = 0)
+constexpr float kRange = 16384.f;   // |value| above which the fp16 split is not used
+
+template <int SUBD>
+struct Cfg {
+    static constexpr int KCOLS = 3 * SUBD + 2;
+    static constexpr int KS = (KCOLS + 15) / 16;   // k-steps of 16
+    static constexpr int KW = KS * 8;              // 32-bit words per A row
+    static constexpr int AST = KW + 1;             // A row stride in words (odd)
+};
+
+// ------------------------------------------------------------ registers <-> memory
+
+template <int E>
+__device__ __forceinline__ void load_halves(const __half *src, float (&f)[E]) {
+    if constexpr (E == 1) {
+        f[0] = __half2float(src[0]);
+    } else if constexpr (E == 2) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
+        f[0] = a.x; f[1] = a.y;
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; j += 4) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(src + j);
+            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+            const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+            f[j] = lo.x; f[j + 1] = lo.y; f[j + 2] = hi.x; f[j + 3] = hi.y;
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void store_halves(__half *dst, const float (&f)[E]) {
+    if constexpr (E == 1) {
+        dst[0] = __float2half_rn(f[0]);
+    } else if constexpr (E == 2) {
+        *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(f[0], f[1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; j += 4) {
+            __half2 lo = __floats2half2_rn(f[j], f[j + 1]);
+            __half2 hi = __floats2half2_rn(f[j + 2], f[j + 3]);
+            uint2 raw;
+            raw.x = *reinterpret_cast<uint32_t *>(&lo);
+            raw.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(dst + j) = raw;
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void load_floats(const float *src, float (&f)[E]) {
+    if constexpr (E == 1) {
+        f[0] = src[0];
+    } else if constexpr (E == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(src);
+        f[0] = a.x; f[1] = a.y;
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; j += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + j);
+            f[j] = a.x; f[j + 1] = a.y; f[j + 2] = a.z; f[j + 3] = a.w;
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void store_floats(float *dst, const float (&f)[E]) {
+    if constexpr (E == 1) {
+        dst[0] = f[0];
+    } else if constexpr (E == 2) {
+        *reinterpret_cast<float2 *>(dst) = make_float2(f[0], f[1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+    }
+}
+
+// Unnormalised Walsh-Hadamard transform (natural order) of the warp's D = 32 E
+// elements, lane holding elements [E lane, E lane + E).  Stage h pairs i with
+// i + h: a, b -> a + b, a - b.  Stages h < E are inside a lane; stage h >= E
+// pairs lane with lane ^ (h / E), where the lower lane keeps own + other and
+// the upper one other - own.
+template <int E>
+__device__ __forceinline__ void reg_fwht(float (&v)[E], int lane) {
+#pragma unroll
+    for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            if (i & h) continue;
+            const float a = v[i], b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const float sg = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = fmaf(sg, v[i], o);
+        }
+    }
+}
+
+__device__ __forceinline__ const float *smooth_row(const EncodeParams &p, int64_t v) {
+    const int h = (int)((v / p.S) % p.H);
+    return p.smooth_mode == 2 ? p.smooth + (size_t)h * p.D : p.smooth;
+}
+
+// Token v -> y = (1/sqrt D) H (s (.) x) (keys) or y = x (values), into yv.
+template <int E>
+__device__ __forceinline__ void forward_token(const EncodeParams &p, int64_t v, float inv_sqrt_d,
+                                              int lane, float *yv) {
+    float f[E];
+    if (v < p.n_vec) {
+        load_halves<E>(p.x + v * p.D + lane * E, f);
+        if (p.rotate) {
+            if (p.smooth_mode != 0) {
+                float s[E];
+                load_floats<E>(smooth_row(p, v) + lane * E, s);
+#pragma unroll
+                for (int j = 0; j < E; ++j) f[j] *= s[j];
+            }
+#pragma unroll
+            for (int j = 0; j < E; ++j) f[j] *= inv_sqrt_d;
+            reg_fwht<E>(f, lane);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) f[j] = 0.f;
+    }
+    store_floats<E>(yv + lane * E, f);
+}
+
+// Chosen centroids in yv -> s^-1 (.) Hn y_hat (keys) or y_hat (values), fp16.
+template <int E>
+__device__ __forceinline__ void inverse_token(const EncodeParams &p, int64_t v, float inv_sqrt_d,
+                                              int lane, const float *yv) {
+    float f[E];
+    load_floats<E>(yv + lane * E, f);
+    if (p.rotate) {
+        reg_fwht<E>(f, lane);
+#pragma unroll
+        for (int j = 0; j < E; ++j) f[j] *= inv_sqrt_d;
+        if (p.smooth_mode != 0) {
+            float s[E];
+            load_floats<E>(smooth_row(p, v) + lane * E, s);
+#pragma unroll
+            for (int j = 0; j < E; ++j) f[j] /= s[j];
+        }
+    }
+    store_halves<E>(p.xhat + v * p.D + lane * E, f);
+}
+
+// ------------------------------------------------------------ screening operands
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
+}
+
+__device__ __forceinline__ uint32_t pack2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+__device__ __forceinline__ __half hi_part(float x) { return __float2half_rn(x); }
+__device__ __forceinline__ __half lo_part(float x) {
+    return __float2half_rn(x - __half2float(__float2half_rn(x)));
+}
+
+// Element k of the screening row of sub-vector y (A operand).
+template <int SUBD>
+__device__ __forceinline__ __half a_val(const float (&y)[SUBD], int k) {
+    if (k < SUBD) return hi_part(y[k]);
+    if (k < 2 * SUBD) return lo_part(y[k - SUBD]);
+    if (k < 3 * SUBD) return hi_part(y[k - 2 * SUBD]);
+    if (k < 3 * SUBD + 2) return __float2half_rn(1.f);
+    return __float2half_rn(0.f);
+}
+
+// Element k of the screening column of centroid c with |c|^2 = n2 (B operand).
+template <int SUBD>
+__device__ __forceinline__ __half b_val(const float *c, float n2, int k) {
+    if (k < SUBD) return __float2half_rn(-2.f * __half2float(hi_part(c[k])));
+    if (k < 2 * SUBD) return __float2half_rn(-2.f * __half2float(hi_part(c[k - SUBD])));
+    if (k < 3 * SUBD) return __float2half_rn(-2.f * __half2float(lo_part(c[k - 2 * SUBD])));
+    if (k == 3 * SUBD) return hi_part(n2);
+    if (k == 3 * SUBD + 1) return lo_part(n2);
+    return __float2half_rn(0.f);
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// (a1 <= a2) and (o1 <= o2), two smallest of disjoint sets -> the two
+// smallest of the union (values are distinct: their tags differ)
+__device__ __forceinline__ void merge_best2(float &a1, float &a2, float o1, float o2) {
+    const float hi = fmaxf(a1, o1);
+    a1 = fminf(a1, o1);
+    a2 = min3f(hi, a2, o2);
+}
+
+// Upper bound on sqrt(x) from the approximate square root (relative error
+// far below the 1e-4 added).
+__device__ __forceinline__ float sqrt_up(float x) {
+    float r;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r * 1.0001f;
+}
+
+// Bound on |f~_c - f_c| for every centroid, |y|^2 = ny2, |c|^2 <= maxn2.
+// Relative part: split residuals and the dropped y_lo c_lo product (each
+// <= 2^-22 of its operand, counted 8 times), fp32 sums of K products
+// allowing truncation (2 K u), both over a generous bound on the sum of
+// term magnitudes (6 |y||c| + 2 |c|^2).  Absolute part: fp16 subnormal
+// spacing (2^-24) in every split, over sum_t |c_t| + |y_t| <= sqrt(SUBD)
+// (|y| + |c|), plus the same for the two norm parts.
+template <int SUBD>
+__device__ __forceinline__ float screen_bound(float ny2, float maxn2, float nc) {
+    constexpr int K = Cfg<SUBD>::KS * 16;
+    const float ny = sqrt_up(ny2);
+    return (2.f * K * kU + 8.f * kU22) * (6.f * ny * nc + 2.f * maxn2) +
+           kU22 * (4.f * sqrtf((float)SUBD) * (ny + nc) + 1.f);
+}
+
+template <int SUBD>
+__device__ __forceinline__ float direct_dist(const float *y, const float *c) {
+    float d = 0.f;
+#pragma unroll
+    for (int t = 0; t < SUBD; ++t) {
+        const float e = y[t] - c[t];
+        d = fmaf(e, e, d);
+    }
+    return d;
+}
+
+template <int SUBD, typename CodeT>
+__global__ void __launch_bounds__(kThr, 3)
+encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
+    using C = Cfg<SUBD>;
+    extern __shared__ __align__(16) float smem[];
+    const int N = p.N, D = p.D;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c4 = lane & 3;
+    // shared memory: fp32 codebook [npad][SUBD] | B fragments [n-tile][k-step]
+    // [lane] | sub-vectors [512][SUBD] | per-warp A rows [32][AST] | max |c|^2,
+    // codebook-range flag
+    const int n_tiles8 = npad / 8;
+    float *cb_s = smem;
+    uint2 *bfrag = reinterpret_cast<uint2 *>(cb_s + npad * SUBD);
+    float *y_s = reinterpret_cast<float *>(bfrag + (size_t)n_tiles8 * C::KS * 32);
+    uint32_t *ascr = reinterpret_cast<uint32_t *>(y_s + kSlots * SUBD);
+    float *misc = reinterpret_cast<float *>(ascr + (kThr / 32) * kPassRows * C::AST);
+    int *bad_cb = reinterpret_cast<int *>(misc + 1);
+
+    if (tid == 0) { misc[0] = 0.f; *bad_cb = 0; }
+    for (int i = tid; i < npad * SUBD; i += kThr) cb_s[i] = i < N * SUBD ? p.codebook[i] : 0.f;
+    __syncthreads();
+    for (int n = tid; n < N; n += kThr) {
+        float n2 = 0.f;
+        bool bad = false;
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) {
+            const float v = cb_s[n * SUBD + t];
+            n2 = fmaf(v, v, n2);
+            bad |= !(fabsf(v) <= kRange);
+        }
+        bad |= !(n2 <= kRange);
+        // non-negative floats order like their bit patterns
+        atomicMax(reinterpret_cast<int *>(&misc[0]), __float_as_int(n2));
+        if (bad) atomicOr(bad_cb, 1);
+    }
+    // B fragments in the order the lanes load them: lane l of n-tile nt holds
+    // centroid nt*8 + l/4 at k = 2(l%4) + {0, 1, 8, 9} of each k-step
+    for (int i = tid; i < n_tiles8 * C::KS * 32; i += kThr) {
+        const int nt = i / (C::KS * 32), rem = i % (C::KS * 32);
+        const int ks = rem / 32, l = rem % 32;
+        const int n = nt * 8 + (l >> 2), k0 = ks * 16 + 2 * (l & 3);
+        const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+        __half v[4];
+        if (n < N) {
+            const float *c = cb_s + n * SUBD;
+            float n2 = 0.f;
+#pragma unroll
+            for (int t = 0; t < SUBD; ++t) n2 = fmaf(c[t], c[t], n2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = b_val<SUBD>(c, n2, kk[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __float2half_rn(kk[j] == 3 * SUBD ? kBigNorm : 0.f);
+        }
+        bfrag[i] = make_uint2(pack2(v[0], v[1]), pack2(v[2], v[3]));
+    }
+    __syncthreads();
+    const float maxn2 = misc[0];
+    const float nc = sqrtf(maxn2) * 1.0001f;
+    const bool cb_bad = *bad_cb != 0;
+    // tag bits: 2 for the quad lane, the rest for the block index; a tagged
+    // value moves by less than 2^tbits ulp, i.e. 2^(tbits - 23) relative
+    const int nblk = npad / kBlockCols;
+    const int tbits = 2 + (nblk > 1 ? 32 - __clz(nblk - 1) : 0);
+    const uint32_t tmask = (1u << tbits) - 1u;
+    const float tag_rel = ldexpf(1.f, tbits - 23);
+
+    const int n_sub = D / SUBD;
+    const int tok = kSlots / n_sub;   // n_sub divides 512
+    const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
+    CodeT *codes = reinterpret_cast<CodeT *>(p.codes);
+    const int64_t lim = p.n_vec * n_sub;
+    uint32_t *arow = ascr + warp * kPassRows * C::AST;
+
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t v0 = tile * tok;
+        // ---- 1. load, smooth, rotate: one warp per token, in registers
+        for (int t = warp; t < tok; t += kThr / 32) {
+            float *yv = y_s + t * D;
+            switch (D) {
+                case 32: forward_token<1>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 64: forward_token<2>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 128: forward_token<4>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 256: forward_token<8>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                default: forward_token<16>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+            }
+        }
+        __syncthreads();
+
+        // ---- 2. nearest centroids, 64 sub-vectors per warp in two passes
+        for (int pass = 0; pass < 2; ++pass) {
+            const int R0 = warp * 64 + pass * kPassRows;
+            // (a) lane l writes the screening row of sub-vector R0 + l
+            {
+                float y[SUBD];
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t) y[t] = y_s[(R0 + lane) * SUBD + t];
+#pragma unroll
+                for (int w = 0; w < C::KW; ++w)
+                    arow[lane * C::AST + w] = pack2(a_val<SUBD>(y, 2 * w), a_val<SUBD>(y, 2 * w + 1));
+            }
+            __syncwarp();
+            uint32_t af[2][C::KS][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    const uint32_t *r0 = arow + (mt * 16 + g) * C::AST + ks * 8;
+                    const uint32_t *r1 = r0 + 8 * C::AST;
+                    af[mt][ks][0] = r0[c4];
+                    af[mt][ks][1] = r1[c4];
+                    af[mt][ks][2] = r0[c4 + 4];
+                    af[mt][ks][3] = r1[c4 + 4];
+                }
+            __syncwarp();
+            // (b) screening.  Row q of this lane: m-tile q/2, row g + 8 (q%2).
+            //     Block minima carry their (block, lane) tag in the low bits.
+            float f1[4], f2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) { f1[q] = INFINITY; f2[q] = INFINITY; }
+            for (int blk = 0; blk < npad / kBlockCols; ++blk) {
+                float bm[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+#pragma unroll
+                for (int j = 0; j < kBlockCols / 8; ++j) {
+                    const int nt = blk * (kBlockCols / 8) + j;
+                    uint2 bf[C::KS];
+#pragma unroll
+                    for (int ks = 0; ks < C::KS; ++ks) bf[ks] = bfrag[(nt * C::KS + ks) * 32 + lane];
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int ks = 0; ks < C::KS; ++ks) mma16816(acc, af[mt][ks], bf[ks]);
+                        bm[2 * mt] = min3f(bm[2 * mt], acc[0], acc[1]);
+                        bm[2 * mt + 1] = min3f(bm[2 * mt + 1], acc[2], acc[3]);
+                    }
+                }
+                const uint32_t tagv = ((uint32_t)blk << 2) | (uint32_t)c4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float t = __uint_as_float((__float_as_uint(bm[q]) & ~tmask) | tagv);
+                    f2[q] = fminf(f2[q], fmaxf(f1[q], t));
+                    f1[q] = fminf(f1[q], t);
+                }
+            }
+            // (c) reduce-scatter over the quad: afterwards quad lane c4 holds the
+            //     merged best and second best of its row q = c4
+            float r1, r2;
+            {
+                const bool b0 = c4 & 1, b1 = (c4 >> 1) & 1;
+                float ka1 = b0 ? f1[1] : f1[0], ka2 = b0 ? f2[1] : f2[0];   // row b0
+                float kb1 = b0 ? f1[3] : f1[2], kb2 = b0 ? f2[3] : f2[2];   // row 2 + b0
+                const float sa1 = b0 ? f1[0] : f1[1], sa2 = b0 ? f2[0] : f2[1];
+                const float sb1 = b0 ? f1[2] : f1[3], sb2 = b0 ? f2[2] : f2[3];
+                merge_best2(ka1, ka2, __shfl_xor_sync(0xffffffffu, sa1, 1),
+                            __shfl_xor_sync(0xffffffffu, sa2, 1));
+                merge_best2(kb1, kb2, __shfl_xor_sync(0xffffffffu, sb1, 1),
+                            __shfl_xor_sync(0xffffffffu, sb2, 1));
+                r1 = b1 ? kb1 : ka1;
+                r2 = b1 ? kb2 : ka2;
+                const float t1 = b1 ? ka1 : kb1, t2 = b1 ? ka2 : kb2;
+                merge_best2(r1, r2, __shfl_xor_sync(0xffffffffu, t1, 2),
+                            __shfl_xor_sync(0xffffffffu, t2, 2));
+            }
+            // (d) direct-form distances of the winner's kBlockCols / 4 candidates
+            //     (its lane's two columns of every n-tile of its block), in
+            //     increasing index order, strict '<': lowest index on ties
+            const int pr = (c4 >> 1) * 16 + g + (c4 & 1) * 8;   // this lane's row
+            int code;
+            bool amb;
+            {
+                float y[SUBD];
+                load_floats<SUBD>(y_s + (R0 + pr) * SUBD, y);
+                const uint32_t tg = __float_as_uint(r1) & tmask;
+                const int nb = (int)(tg >> 2) * kBlockCols + 2 * (int)(tg & 3);
+                float b = INFINITY;
+                int bi = 0;
+#pragma unroll
+                for (int j = 0; j < kBlockCols / 8; ++j) {
+#pragma unroll
+                    for (int col = 0; col < 2; ++col) {
+                        const int n = nb + j * 8 + col;
+                        if (n < N) {
+                            float c[SUBD];
+                            load_floats<SUBD>(cb_s + n * SUBD, c);
+                            float d = 0.f;
+#pragma unroll
+                            for (int t = 0; t < SUBD; ++t) {
+                                const float e = y[t] - c[t];
+                                d = fmaf(e, e, d);
+                            }
+                            if (d < b) { b = d; bi = n; }
+                        }
+                    }
+                }
+                float ny2 = 0.f;
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t) ny2 = fmaf(y[t], y[t], ny2);
+                // every other candidate: screened value >= untagged r2, exact
+                // distance >= that + |y|^2 - E, and its direct form within
+                // (SUBD + 3) u of the exact one (ny2 within SUBD u)
+                const float E = screen_bound<SUBD>(ny2, maxn2, nc);
+                const float outside = r2 + ny2;
+                const float margin = E + tag_rel * fabsf(r2) +
+                                     (4.f * SUBD + 8.f) * kU * (fabsf(outside) + b + ny2 + maxn2);
+                const bool live = v0 * n_sub + R0 + pr < lim;
+                amb = live && (cb_bad || !(ny2 <= kRange * kRange) || !(b < INFINITY) ||
+                               !(outside - b > margin));
+                code = bi;
+            }
+            // (e) ambiguous rows: the whole warp rescans the row in the direct form
+            {
+                unsigned m = __ballot_sync(0xffffffffu, amb);
+                while (m) {
+                    const int src = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int sc = src & 3;
+                    const int spr = (sc >> 1) * 16 + (src >> 2) + (sc & 1) * 8;
+                    const float *yr = y_s + (R0 + spr) * SUBD;
+                    float best = INFINITY;
+                    int bi = 0x7fffffff;
+                    for (int n = lane; n < N; n += 32) {
+                        const float d = direct_dist<SUBD>(yr, cb_s + n * SUBD);
+                        if (d < best) { best = d; bi = n; }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                        if (ob < best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+                    }
+                    if (lane == src) code = bi == 0x7fffffff ? 0 : bi;
+                }
+            }
+            // (f) lane l takes the code of row l (held by quad lane q of quad
+            //     l % 8): coalesced store; the chosen centroid replaces the
+            //     sub-vector for the reconstruction
+            const int mine = __shfl_sync(0xffffffffu, code,
+                                         (lane & 7) * 4 + (((lane >> 4) << 1) | ((lane >> 3) & 1)));
+            const int64_t gi = v0 * n_sub + R0 + lane;
+            if (gi < lim) codes[gi] = (CodeT)mine;
+            __syncwarp();
+            if (p.xhat) {
+#pragma unroll
+                for (int t = 0; t < SUBD; ++t)
+                    y_s[(R0 + lane) * SUBD + t] = cb_s[mine * SUBD + t];
+            }
+        }
+        __syncthreads();
+
+        // ---- 3. optional reconstruction -> fp16
+        if (p.xhat) {
+            for (int t = warp; t < tok; t += kThr / 32) {
+                const int64_t v = v0 + t;
+                if (v >= p.n_vec) continue;   // warp-uniform
+                const float *yv = y_s + t * D;
+                switch (D) {
+                    case 32: inverse_token<1>(p, v, inv_sqrt_d, lane, yv); break;
+                    case 64: inverse_token<2>(p, v, inv_sqrt_d, lane, yv); break;
+                    case 128: inverse_token<4>(p, v, inv_sqrt_d, lane, yv); break;
+                    case 256: inverse_token<8>(p, v, inv_sqrt_d, lane, yv); break;
+                    default: inverse_token<16>(p, v, inv_sqrt_d, lane, yv); break;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int SUBD>
+size_t mma_smem_bytes(int npad) {
+    using C = Cfg<SUBD>;
+    return sizeof(float) * (size_t)npad * SUBD + sizeof(uint2) * (size_t)(npad / 8) * C::KS * 32 +
+           sizeof(float) * (size_t)kSlots * SUBD +
+           sizeof(uint32_t) * (size_t)(kThr / 32) * kPassRows * C::AST + 16;
+}
+
+template <int SUBD, typename CodeT>
+cudaError_t launch_t(const EncodeParams &p, cudaStream_t stream) {
+    const int npad = (p.N + kBlockCols - 1) & ~(kBlockCols - 1);
+    const size_t smem = mma_smem_bytes<SUBD>(npad);
+    auto kern = encode_mma_kernel<SUBD, CodeT>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThr, smem)) !=
+        cudaSuccess)
+        return err;
+    if (per_sm < 1) per_sm = 1;
+    const int n_sub = p.D / SUBD;
+    const int64_t tok = kSlots / n_sub;
+    const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > n_tiles) grid = n_tiles;
+    const float inv_sqrt_d = (float)(1.0 / sqrt((double)p.D));
+    kern<<<(unsigned)grid, kThr, smem, stream>>>(p, inv_sqrt_d, npad);
+    return cudaGetLastError();
+}
+
+template <int SUBD>
+cudaError_t launch_c(const EncodeParams &p, cudaStream_t s) {
+    return p.code_bytes == 1 ? launch_t<SUBD, uint8_t>(p, s) : launch_t<SUBD, uint16_t>(p, s);
+}
+
+}  // namespace
+
+bool encode_mma_supported(int N, int sub_dim) {
+    const int npad = (N + kBlockCols - 1) & ~(kBlockCols - 1);
+    size_t bytes = 0;
+    switch (sub_dim) {
+        case 2: bytes = mma_smem_bytes<2>(npad); break;
+        case 4: bytes = mma_smem_bytes<4>(npad); break;
+        case 8: bytes = mma_smem_bytes<8>(npad); break;
+        default: return false;
+    }
+    return bytes <= 200u * 1024u;
+}
+
+cudaError_t launch_encode_mma(const EncodeParams &p, cudaStream_t stream) {
+    switch (p.sub_dim) {
+        case 2: return launch_c<2>(p, stream);
+        case 4: return launch_c<4>(p, stream);
+        case 8: return launch_c<8>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vqkv

@@ -27,6 +27,10 @@ struct EncodeParams {
 // Returns a cudaError_t of the launch.
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream);
 size_t encode_smem_bytes(int N, int sub_dim);
+// Tensor-core screening variant (sub_dim 2, 4, 8 with the codebook's
+// operands fitting in shared memory); launch_encode dispatches to it.
+bool encode_mma_supported(int N, int sub_dim);
+cudaError_t launch_encode_mma(const EncodeParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- dequant
 struct DequantParams {

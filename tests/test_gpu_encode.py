@@ -26,6 +26,7 @@ CASES = [
     (512, 16, 128, 2, 1, 1, 9),      # one token per tile
     (128, 1, 32, 2, 1, 1, 12),
     (64, 16, 512, 1, 1, 2, 50),
+    (64, 4, 4096, 2, 1, 1, 40),      # codebook too large for the tensor-core screen
 ]
 
 
@@ -137,3 +138,44 @@ def test_encode_full_size_sampled(name):
     rv = check_encode(inp["values"], inp["v_codebook"], spec.v_d, None, False,
                       vc.cpu().numpy(), None, rows=rows)
     print(name, "keys", rk, "values", rv)
+
+
+def _encode_case(seed, D, d, N, x_scale, cb_scale, H=2, S=70, cb=None):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((1, H, S, D)) * x_scale).astype(np.float16)
+    if cb is None:
+        cb = (rng.standard_normal((N, d)) * cb_scale).astype(np.float32)
+    smooth = rng.uniform(0.5, 2.0, (H, D)).astype(np.float32)
+    kc, kh = vq.encode_keys(dev(x), dev(cb), d, dev(smooth), want_k_hat=True)
+    torch.cuda.synchronize()
+    res = check_encode(x, cb, d, smooth, True, kc.cpu().numpy(), kh.cpu().numpy())
+    return kc.cpu().numpy().astype(np.int64), res
+
+
+@pytest.mark.parametrize("D,d,N,x_scale,cb_scale", [
+    (128, 4, 100, 1.0, 1.0),       # N not a multiple of 32: padded columns
+    (64, 2, 1, 1.0, 1.0),          # a single centroid
+    (128, 8, 33, 1.0, 1.0),
+    (256, 2, 256, 1.0, 1.0),
+    (128, 4, 256, 3000.0, 3000.0), # beyond the range of the fp16 operand split
+    (128, 4, 256, 3000.0, 1.0),    # large sub-vectors, ordinary codebook
+    (64, 4, 256, 1e-4, 1e-4),      # fp16-subnormal split parts
+])
+def test_encode_screening_edge_cases(D, d, N, x_scale, cb_scale):
+    codes, res = _encode_case(D + N + d, D, d, N, x_scale, cb_scale)
+    assert res["mismatch"] == res["near_tie"] + res["fp32_bound"], res
+    if N == 1:
+        assert (codes == 0).all()
+
+
+@pytest.mark.parametrize("layout", ["adjacent", "far"])
+def test_encode_duplicate_centroids_take_lowest_index(layout):
+    """Exact duplicates tie in every arithmetic; the lower index must win."""
+    rng = np.random.default_rng(31)
+    base = rng.standard_normal((128, 4)).astype(np.float32)
+    cb = np.repeat(base, 2, axis=0) if layout == "adjacent" else np.concatenate([base, base])
+    codes, res = _encode_case(32, 128, 4, 256, 1.0, 1.0, cb=cb)
+    if layout == "adjacent":
+        assert (codes % 2 == 0).all()
+    else:
+        assert (codes < 128).all()
