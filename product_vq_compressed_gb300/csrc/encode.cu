@@ -114,7 +114,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
             float *yv = y_s + t * D;
             if (v < p.n_vec) {
                 const __half *xv = p.x + v * D;
-                const int h = (int)((v / p.S) % p.H);
+                const int h = token_head(p, v);
                 const float *sm = p.smooth_mode == 2 ? p.smooth + (size_t)h * D
                                                      : p.smooth;
                 for (int e = lane * 4; e < D; e += 128) {
@@ -264,7 +264,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                 if (v >= p.n_vec) continue;
                 float *yv = y_s + t * D;
                 if (p.rotate) warp_fwht(yv, D, lane);
-                const int h = (int)((v / p.S) % p.H);
+                const int h = token_head(p, v);
                 const float *sm = p.smooth_mode == 2 ? p.smooth + (size_t)h * D
                                                      : p.smooth;
                 __half *ov = p.xhat + v * D;

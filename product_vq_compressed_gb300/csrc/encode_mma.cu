@@ -47,7 +47,9 @@ constexpr int kPassRows = 32;       // rows per warp pass (two 16-row m-tiles)
 constexpr int kBlockCols = 64;      // centroids per screening block (8 n-tiles)
 constexpr float kU = 5.9604645e-8f;    // 2^-24
 constexpr float kU22 = 2.3841858e-7f;  // 2^-22
-constexpr float kBigNorm = 30000.f; // |c|^2 of padding centroids (c = 0)
+constexpr float kBigNorm = 30000.f; // screened |c|^2 of padding centroids
+constexpr float kFarCoord = 1e18f;  // exact-step coordinates of padding centroids
+constexpr float kFarDist = 1e30f;   // direct distances at or above this: padding
 constexpr float kRange = 16384.f;   // |value| above which the fp16 split is not used
 
 template <int SUBD>
@@ -57,6 +59,11 @@ struct Cfg {
     static constexpr int KW = KS * 8;              // 32-bit words per A row
     static constexpr int AST = KW + 1;             // A row stride in words (odd)
 };
+
+// Shared-memory row of centroid n: its low three bits are xor-ed with the
+// screening block, so that lanes reading the winners of different blocks in
+// the exact step spread over the banks.  A permutation within groups of 8.
+__device__ __forceinline__ int cslot(int n) { return n ^ ((n / kBlockCols) & 7); }
 
 // ------------------------------------------------------------ registers <-> memory
 
@@ -155,7 +162,7 @@ __device__ __forceinline__ void reg_fwht(float (&v)[E], int lane) {
 }
 
 __device__ __forceinline__ const float *smooth_row(const EncodeParams &p, int64_t v) {
-    const int h = (int)((v / p.S) % p.H);
+    const int h = token_head(p, v);
     return p.smooth_mode == 2 ? p.smooth + (size_t)h * p.D : p.smooth;
 }
 
@@ -250,6 +257,34 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
     return r;
 }
 
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// sum_t (y_t - c_t)^2 in fp32 with packed two-wide operations: the even and
+// the odd dimensions are accumulated separately and added at the end.
+// y holds the sub-vector as (y0, y1), (y2, y3), ...
+template <int SUBD>
+__device__ __forceinline__ float pair_dist(const unsigned long long (&y)[SUBD / 2], const float *cp) {
+    float c[SUBD];
+    load_floats<SUBD>(cp, c);
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int i = 0; i < SUBD / 2; ++i) {
+        unsigned long long e;
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(e) : "l"(y[i]), "l"(pack_f2(c[2 * i], c[2 * i + 1])));
+        if (i == 0)
+            asm("mul.rn.f32x2 %0, %1, %1;" : "=l"(acc) : "l"(e));
+        else
+            asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(acc) : "l"(e), "l"(acc));
+    }
+    float a0, a1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+    return a0 + a1;
+}
+
 // (a1 <= a2) and (o1 <= o2), two smallest of disjoint sets -> the two
 // smallest of the union (values are distinct: their tags differ)
 __device__ __forceinline__ void merge_best2(float &a1, float &a2, float o1, float o2) {
@@ -300,7 +335,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     const int N = p.N, D = p.D;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    // shared memory: fp32 codebook [npad][SUBD] | B fragments [n-tile][k-step]
+    // shared memory: fp32 codebook [npad][SUBD] (row cslot(n)) | B fragments [n-tile][k-step]
     // [lane] | sub-vectors [512][SUBD] | per-warp A rows [32][AST] | max |c|^2,
     // codebook-range flag
     const int n_tiles8 = npad / 8;
@@ -312,14 +347,15 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     int *bad_cb = reinterpret_cast<int *>(misc + 1);
 
     if (tid == 0) { misc[0] = 0.f; *bad_cb = 0; }
-    for (int i = tid; i < npad * SUBD; i += kThr) cb_s[i] = i < N * SUBD ? p.codebook[i] : 0.f;
+    for (int i = tid; i < npad * SUBD; i += kThr)
+        cb_s[cslot(i / SUBD) * SUBD + i % SUBD] = i < N * SUBD ? p.codebook[i] : kFarCoord;
     __syncthreads();
     for (int n = tid; n < N; n += kThr) {
         float n2 = 0.f;
         bool bad = false;
 #pragma unroll
         for (int t = 0; t < SUBD; ++t) {
-            const float v = cb_s[n * SUBD + t];
+            const float v = cb_s[cslot(n) * SUBD + t];
             n2 = fmaf(v, v, n2);
             bad |= !(fabsf(v) <= kRange);
         }
@@ -337,7 +373,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
         const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
         __half v[4];
         if (n < N) {
-            const float *c = cb_s + n * SUBD;
+            const float *c = cb_s + cslot(n) * SUBD;
             float n2 = 0.f;
 #pragma unroll
             for (int t = 0; t < SUBD; ++t) n2 = fmaf(c[t], c[t], n2);
@@ -466,28 +502,24 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             {
                 float y[SUBD];
                 load_floats<SUBD>(y_s + (R0 + pr) * SUBD, y);
+                unsigned long long y2[SUBD / 2];
+#pragma unroll
+                for (int i = 0; i < SUBD / 2; ++i) y2[i] = pack_f2(y[2 * i], y[2 * i + 1]);
                 const uint32_t tg = __float_as_uint(r1) & tmask;
                 const int nb = (int)(tg >> 2) * kBlockCols + 2 * (int)(tg & 3);
+                const int sb = cslot(nb);   // slots of nb + 8 j + col: (sb + 8 j) ^ col
+                // padding candidates (index >= N) sit at kFarCoord: d >= kFarDist
                 float b = INFINITY;
-                int bi = 0;
+                int bj = 0;
 #pragma unroll
                 for (int j = 0; j < kBlockCols / 8; ++j) {
 #pragma unroll
                     for (int col = 0; col < 2; ++col) {
-                        const int n = nb + j * 8 + col;
-                        if (n < N) {
-                            float c[SUBD];
-                            load_floats<SUBD>(cb_s + n * SUBD, c);
-                            float d = 0.f;
-#pragma unroll
-                            for (int t = 0; t < SUBD; ++t) {
-                                const float e = y[t] - c[t];
-                                d = fmaf(e, e, d);
-                            }
-                            if (d < b) { b = d; bi = n; }
-                        }
+                        const float d = pair_dist<SUBD>(y2, cb_s + ((sb + j * 8) ^ col) * SUBD);
+                        if (d < b) { b = d; bj = 8 * j + col; }
                     }
                 }
+                const int bi = nb + bj;
                 float ny2 = 0.f;
 #pragma unroll
                 for (int t = 0; t < SUBD; ++t) ny2 = fmaf(y[t], y[t], ny2);
@@ -499,7 +531,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                 const float margin = E + tag_rel * fabsf(r2) +
                                      (4.f * SUBD + 8.f) * kU * (fabsf(outside) + b + ny2 + maxn2);
                 const bool live = v0 * n_sub + R0 + pr < lim;
-                amb = live && (cb_bad || !(ny2 <= kRange * kRange) || !(b < INFINITY) ||
+                amb = live && (cb_bad || !(ny2 <= kRange * kRange) || !(b < kFarDist) ||
                                !(outside - b > margin));
                 code = bi;
             }
@@ -515,7 +547,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                     float best = INFINITY;
                     int bi = 0x7fffffff;
                     for (int n = lane; n < N; n += 32) {
-                        const float d = direct_dist<SUBD>(yr, cb_s + n * SUBD);
+                        const float d = direct_dist<SUBD>(yr, cb_s + cslot(n) * SUBD);
                         if (d < best) { best = d; bi = n; }
                     }
 #pragma unroll
@@ -538,7 +570,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             if (p.xhat) {
 #pragma unroll
                 for (int t = 0; t < SUBD; ++t)
-                    y_s[(R0 + lane) * SUBD + t] = cb_s[mine * SUBD + t];
+                    y_s[(R0 + lane) * SUBD + t] = cb_s[cslot(mine) * SUBD + t];
             }
         }
         __syncthreads();

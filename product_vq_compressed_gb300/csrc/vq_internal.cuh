@@ -10,6 +10,25 @@
 
 namespace vqkv {
 
+// ---------------------------------------------------------------- helpers
+// Division by an invariant 32-bit divisor d >= 1 as a multiply-high, add and
+// shift (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994, the round-up method): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(m, n) + n) >> l for every
+// n < 2^31 (the sum stays below 2^32).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d, 0u, 0u};
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = (uint32_t)((((1ull << f.l) - d) << 32) / d + 1);
+    return f;
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
+    return (__umulhi(f.m, n) + n) >> f.l;
+}
+
 // ---------------------------------------------------------------- encode
 struct EncodeParams {
     const __half *x;          // [n_vec, D]
@@ -23,7 +42,17 @@ struct EncodeParams {
     void *codes;              // [n_vec, D/sub_dim], code_bytes each
     int code_bytes;
     __half *xhat;             // [n_vec, D] or null
+    FastDiv div_S, div_H;     // by S and H (head of a token)
 };
+
+// Head of token v of a [B, H, S, D] tensor: (v / S) mod H.
+__device__ __forceinline__ int token_head(const EncodeParams &p, int64_t v) {
+    if (p.n_vec < (int64_t(1) << 31)) {
+        const uint32_t q = fast_div((uint32_t)v, p.div_S);
+        return (int)(q - fast_div(q, p.div_H) * (uint32_t)p.H);
+    }
+    return (int)((v / p.S) % p.H);
+}
 // Returns a cudaError_t of the launch.
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream);
 size_t encode_smem_bytes(int N, int sub_dim);

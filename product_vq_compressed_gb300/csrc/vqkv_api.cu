@@ -61,6 +61,8 @@ int encode_common(const void *x, int B, int H, int S, int D,
     p.codes = codes;
     p.code_bytes = code_bytes;
     p.xhat = reinterpret_cast<__half *>(xhat);
+    p.div_S = vqkv::make_fastdiv((uint32_t)(S > 0 ? S : 1));
+    p.div_H = vqkv::make_fastdiv((uint32_t)(H > 0 ? H : 1));
     return vqkv::launch_encode(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VQ_OK
                : VQ_ERR_CUDA;
