@@ -175,6 +175,25 @@ __device__ __forceinline__ void gather_sh(uint32_t addr, uint32_t *w) {
 
 constexpr uint32_t kFastRow = 256;                 // bytes per interleaved row
 
+// 16 bytes of fp16 copies of the centroid at c (SUB fp32 values): words
+// (c0 c1), (c2 c3), ... repeated to fill the chunk.
+template <int SUB>
+__device__ __forceinline__ uint4 replica_chunk(const float *c) {
+    if constexpr (SUB == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(c);
+        const uint32_t w = pack_h2(v.x, v.y);
+        return make_uint4(w, w, w, w);
+    } else if constexpr (SUB == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(c);
+        const uint32_t w0 = pack_h2(v.x, v.y), w1 = pack_h2(v.z, v.w);
+        return make_uint4(w0, w1, w0, w1);
+    } else {
+        const float4 v = *reinterpret_cast<const float4 *>(c);
+        const float4 u = *reinterpret_cast<const float4 *>(c + 4);
+        return make_uint4(pack_h2(v.x, v.y), pack_h2(v.z, v.w), pack_h2(u.x, u.y), pack_h2(u.z, u.w));
+    }
+}
+
 __host__ __device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
 // ------------------------------------------------------------- the kernel
@@ -215,7 +234,6 @@ __host__ __device__ __forceinline__ int64_t share_start(int64_t gw, int64_t shar
 
 template <int D>
 struct WarpScratch {
-    float work[D];            // fp32 FWHT buffer for one query column
     __half qt[kCols][D];      // transformed queries (fp16 MMA operands)
     int lo[kCols], hi[kCols]; // visible key range per column
 };
@@ -473,23 +491,38 @@ decode_kernel(DecArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, c4 = lane & 3;
 
-    // ---- stage both codebooks: fp32 copy (coalesced), then fp16 tables
-    //      replicated per bank group (rows past N are zero on the fast path)
-    const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
-    for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
-    for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
-    __syncthreads();
-    for (int i = tid; i < nk_rows * (krow / 4); i += kThreads) {
-        const int c = i / (krow / 4), wi = i % (krow / 4);
-        const int t = ((wi * 4) % EK) / 2;
-        *reinterpret_cast<uint32_t *>(ktab + (size_t)c * kstride + wi * 4) =
-            c < a.Nk ? pack_h2(stage[c * DK + t], stage[c * DK + t + 1]) : 0u;
-    }
-    for (int i = tid; i < nv_rows * (vrow / 4); i += kThreads) {
-        const int c = i / (vrow / 4), wi = i % (vrow / 4);
-        const int t = ((wi * 4) % EV) / 2;
-        *reinterpret_cast<uint32_t *>(vtab + (size_t)c * vstride + wi * 4) =
-            c < a.Nv ? pack_h2(stage[nk_f + c * DV + t], stage[nk_f + c * DV + t + 1]) : 0u;
+    // ---- fp16 tables replicated per bank group (rows past N are zero)
+    if constexpr (FAST) {
+        // 256 rows x 16 chunks of 16 bytes (8 key, 8 value); every chunk of a
+        // row half holds 16 / EK (16 / EV) copies of its centroid
+        for (int i = tid; i < 256 * 16; i += kThreads) {
+            const int c = i >> 4, q = i & 15;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (q < 8) {
+                if (c < a.Nk) w = replica_chunk<DK>(a.kcbk + c * DK);
+            } else {
+                if (c < a.Nv) w = replica_chunk<DV>(a.vcbk + c * DV);
+            }
+            *reinterpret_cast<uint4 *>(ktab + c * kFastRow + q * 16) = w;
+        }
+    } else {
+        // fp32 copy (coalesced), then the tables word by word
+        const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
+        for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
+        for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
+        __syncthreads();
+        for (int i = tid; i < nk_rows * (krow / 4); i += kThreads) {
+            const int c = i / (krow / 4), wi = i % (krow / 4);
+            const int t = ((wi * 4) % EK) / 2;
+            *reinterpret_cast<uint32_t *>(ktab + (size_t)c * kstride + wi * 4) =
+                c < a.Nk ? pack_h2(stage[c * DK + t], stage[c * DK + t + 1]) : 0u;
+        }
+        for (int i = tid; i < nv_rows * (vrow / 4); i += kThreads) {
+            const int c = i / (vrow / 4), wi = i % (vrow / 4);
+            const int t = ((wi * 4) % EV) / 2;
+            *reinterpret_cast<uint32_t *>(vtab + (size_t)c * vstride + wi * 4) =
+                c < a.Nv ? pack_h2(stage[nk_f + c * DV + t], stage[nk_f + c * DV + t + 1]) : 0u;
+        }
     }
     __syncthreads();
     const uint32_t klane = (uint32_t)((lane % a.k_copies) * EK);
@@ -523,22 +556,21 @@ decode_kernel(DecArgs a) {
                 const int hq = g * a.G + gam;
                 const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + i) * D;
                 const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * D : a.smooth;
-                for (int e = lane; e < D; e += 32) {
-                    float v = __half2float(qp[e]);
-                    if (a.smooth_mode != 0) v = v / sp[e];
-                    ws.work[e] = v * a.inv_sqrt_d;
+                // lane holds dims [E lane, E lane + E); FWHT by butterflies in
+                // registers and xor-shuffles
+                constexpr int E = D / 32;
+                float f[E];
+                load_halves<E>(qp + lane * E, f);
+                if (a.smooth_mode != 0) {
+                    float sv[E];
+                    load_floats<E>(sp + lane * E, sv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) f[e] = f[e] / sv[e];
                 }
-                __syncwarp();
-                for (int h = 1; h < D; h <<= 1) {
-                    for (int p = lane; p < D / 2; p += 32) {
-                        const int x = ((p & ~(h - 1)) << 1) | (p & (h - 1));
-                        const float uu = ws.work[x], w = ws.work[x + h];
-                        ws.work[x] = uu + w;
-                        ws.work[x + h] = uu - w;
-                    }
-                    __syncwarp();
-                }
-                for (int e = lane; e < D; e += 32) ws.qt[col][e] = __float2half_rn(ws.work[e]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) f[e] *= a.inv_sqrt_d;
+                reg_fwht<E>(f, lane);
+                store_halves<E>(ws.qt[col] + lane * E, f);
                 if (lane == 0) {
                     const int q_abs = a.S_kv - a.S_q + i;
                     int hi = a.causal ? q_abs : a.S_kv - 1;
@@ -630,20 +662,22 @@ decode_kernel(DecArgs a) {
             us.l0 += __shfl_xor_sync(0xffffffffu, us.l0, off);
             us.l1 += __shfl_xor_sync(0xffffffffu, us.l1, off);
         }
+        // (columns past the last real one have no record: the combine skips them)
         float *rec = a.ws + ((gw * a.slots + slot) * kCols) * (int64_t)(D + 4);
+        float *rec0 = rec + (2 * c4) * (D + 4), *rec1 = rec0 + (D + 4);
+        const bool real0 = cblk * kCols + 2 * c4 < n_cols_total;
+        const bool real1 = cblk * kCols + 2 * c4 + 1 < n_cols_total;
         if (g8 == 0) {
-            rec[(2 * c4) * (D + 4)] = us.m0;
-            rec[(2 * c4) * (D + 4) + 1] = us.l0;
-            rec[(2 * c4 + 1) * (D + 4)] = us.m1;
-            rec[(2 * c4 + 1) * (D + 4) + 1] = us.l1;
+            if (real0) *reinterpret_cast<float2 *>(rec0) = make_float2(us.m0, us.l0);
+            if (real1) *reinterpret_cast<float2 *>(rec1) = make_float2(us.m1, us.l1);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const int d0 = g8 * (D / 8) + 2 * mt;
-            rec[(2 * c4) * (D + 4) + 4 + d0] = us.acc_o[mt][0];
-            rec[(2 * c4 + 1) * (D + 4) + 4 + d0] = us.acc_o[mt][1];
-            rec[(2 * c4) * (D + 4) + 4 + d0 + 1] = us.acc_o[mt][2];
-            rec[(2 * c4 + 1) * (D + 4) + 4 + d0 + 1] = us.acc_o[mt][3];
+            if (real0)
+                *reinterpret_cast<float2 *>(rec0 + 4 + d0) = make_float2(us.acc_o[mt][0], us.acc_o[mt][2]);
+            if (real1)
+                *reinterpret_cast<float2 *>(rec1 + 4 + d0) = make_float2(us.acc_o[mt][1], us.acc_o[mt][3]);
         }
         ++slot;
         t = seg_end;
@@ -651,21 +685,23 @@ decode_kernel(DecArgs a) {
 }
 
 // Merge the partial records of every (unit, column) and write fp16.  The
-// records of a unit come from the warps whose shares overlap it.  The block
-// (256 threads) reduces their maxima and sums in parallel and keeps each
-// record's rescale factor in shared memory; then 256 / D groups of D threads
-// (one output dimension each) accumulate disjoint subsets of the records with
-// many loads in flight, and the groups' sums are added.
+// records of a unit come from the warps whose shares overlap it.  Block
+// (unit, column, chunk of kCombDims output dimensions), 256 threads: the
+// block reduces the records' maxima and sums in parallel and keeps each
+// record's rescale factor in shared memory; then 8 groups of kCombDims
+// threads (one output dimension each) accumulate disjoint subsets of the
+// records with many loads in flight, and the groups' sums are added.
 constexpr int kCombThreads = 256;
+constexpr int kCombDims = 32;
 constexpr int kMaxRecords = 2048;   // >= warps of any plan (one CTA per SM)
 
 template <int D>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(DecArgs a, __half *__restrict__ out) {
-    constexpr int kGroups = kCombThreads / D;
+    constexpr int kGroups = kCombThreads / kCombDims;
     __shared__ float fac[kMaxRecords];
     __shared__ float red[kCombThreads / 32];
-    __shared__ float part[kGroups][D];
+    __shared__ float part[kGroups][kCombDims];
     const int64_t unit = blockIdx.x;
     const int col = blockIdx.y;
     const int cblk = (int)(unit % a.n_colblk);
@@ -675,7 +711,7 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
     const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
     const int i = cg / a.G, gam = cg % a.G;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = tid % D, grp = tid / D;
+    const int d = (int)blockIdx.z * kCombDims + tid % kCombDims, grp = tid / kCombDims;
     const int64_t u0 = unit * a.T;
     const int64_t w_lo = u0 / a.share;
     int64_t w_hi = (u0 + a.T - 1) / a.share;
@@ -721,11 +757,11 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
         l = block_reduce(l, false);   // its barriers also publish fac[]
 #pragma unroll 8
         for (int k = grp; k < n_rec; k += kGroups) o += fac[k] * rec_of(k)[4 + d];
-        part[grp][d] = o;
+        part[grp][tid % kCombDims] = o;
         __syncthreads();
         o = 0.f;
 #pragma unroll
-        for (int q = 0; q < kGroups; ++q) o += part[q][d];
+        for (int q = 0; q < kGroups; ++q) o += part[q][tid % kCombDims];
         o = l > 0.f ? o / l : 0.f;
     }
     if (grp == 0) {
@@ -939,7 +975,8 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     }
     if (err != cudaSuccess) return err;
     const int64_t units = plan.total / plan.tiles;
-    dim3 cgrid((unsigned)units, kCols);
+    const int cols = min(kCols, da.G * da.S_q);   // real columns of a column block
+    dim3 cgrid((unsigned)units, (unsigned)cols, (unsigned)(a.D / kCombDims));
     __half *out = reinterpret_cast<__half *>(a.out_f16);
     switch (a.D) {
         case 32: combine_kernel<32><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;

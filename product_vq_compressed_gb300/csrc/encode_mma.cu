@@ -65,102 +65,6 @@ struct Cfg {
 // the exact step spread over the banks.  A permutation within groups of 8.
 __device__ __forceinline__ int cslot(int n) { return n ^ ((n / kBlockCols) & 7); }
 
-// ------------------------------------------------------------ registers <-> memory
-
-template <int E>
-__device__ __forceinline__ void load_halves(const __half *src, float (&f)[E]) {
-    if constexpr (E == 1) {
-        f[0] = __half2float(src[0]);
-    } else if constexpr (E == 2) {
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
-        f[0] = a.x; f[1] = a.y;
-    } else {
-#pragma unroll
-        for (int j = 0; j < E; j += 4) {
-            const uint2 raw = *reinterpret_cast<const uint2 *>(src + j);
-            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-            const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-            f[j] = lo.x; f[j + 1] = lo.y; f[j + 2] = hi.x; f[j + 3] = hi.y;
-        }
-    }
-}
-
-template <int E>
-__device__ __forceinline__ void store_halves(__half *dst, const float (&f)[E]) {
-    if constexpr (E == 1) {
-        dst[0] = __float2half_rn(f[0]);
-    } else if constexpr (E == 2) {
-        *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(f[0], f[1]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < E; j += 4) {
-            __half2 lo = __floats2half2_rn(f[j], f[j + 1]);
-            __half2 hi = __floats2half2_rn(f[j + 2], f[j + 3]);
-            uint2 raw;
-            raw.x = *reinterpret_cast<uint32_t *>(&lo);
-            raw.y = *reinterpret_cast<uint32_t *>(&hi);
-            *reinterpret_cast<uint2 *>(dst + j) = raw;
-        }
-    }
-}
-
-template <int E>
-__device__ __forceinline__ void load_floats(const float *src, float (&f)[E]) {
-    if constexpr (E == 1) {
-        f[0] = src[0];
-    } else if constexpr (E == 2) {
-        const float2 a = *reinterpret_cast<const float2 *>(src);
-        f[0] = a.x; f[1] = a.y;
-    } else {
-#pragma unroll
-        for (int j = 0; j < E; j += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(src + j);
-            f[j] = a.x; f[j + 1] = a.y; f[j + 2] = a.z; f[j + 3] = a.w;
-        }
-    }
-}
-
-template <int E>
-__device__ __forceinline__ void store_floats(float *dst, const float (&f)[E]) {
-    if constexpr (E == 1) {
-        dst[0] = f[0];
-    } else if constexpr (E == 2) {
-        *reinterpret_cast<float2 *>(dst) = make_float2(f[0], f[1]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < E; j += 4)
-            *reinterpret_cast<float4 *>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
-    }
-}
-
-// Unnormalised Walsh-Hadamard transform (natural order) of the warp's D = 32 E
-// elements, lane holding elements [E lane, E lane + E).  Stage h pairs i with
-// i + h: a, b -> a + b, a - b.  Stages h < E are inside a lane; stage h >= E
-// pairs lane with lane ^ (h / E), where the lower lane keeps own + other and
-// the upper one other - own.
-template <int E>
-__device__ __forceinline__ void reg_fwht(float (&v)[E], int lane) {
-#pragma unroll
-    for (int h = 1; h < E; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            if (i & h) continue;
-            const float a = v[i], b = v[i + h];
-            v[i] = a + b;
-            v[i + h] = a - b;
-        }
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const float sg = (lane & m) ? -1.f : 1.f;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = fmaf(sg, v[i], o);
-        }
-    }
-}
-
 __device__ __forceinline__ const float *smooth_row(const EncodeParams &p, int64_t v) {
     const int h = token_head(p, v);
     return p.smooth_mode == 2 ? p.smooth + (size_t)h * p.D : p.smooth;
