@@ -29,6 +29,12 @@
  *     validated on the host before anything is enqueued, so an error status
  *     means nothing was launched (except VQ_ERR_CUDA, which reports a failed
  *     launch).
+ *   - The attention kernels are launched as programmatic dependents: when
+ *     the preceding work on the stream is a vq_encode_* call, they may start
+ *     staging their codebooks while that encode finishes, and read every
+ *     other input (codes, queries, smooth factors) only after it completed.
+ *     So an attention call's codebooks must not be outputs of the encode call
+ *     enqueued just before it (codes and reconstructions never are).
  *   - The library never aborts, exits or traps on the device.
  */
 #ifndef VQKV_H_

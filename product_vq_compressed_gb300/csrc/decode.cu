@@ -490,6 +490,8 @@ decode_kernel(DecArgs a) {
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, c4 = lane & 3;
+    // the combine may be scheduled now; it waits for this grid to finish
+    pdl_launch_dependents();
 
     // ---- fp16 tables replicated per bank group (rows past N are zero)
     if constexpr (FAST) {
@@ -525,6 +527,9 @@ decode_kernel(DecArgs a) {
         }
     }
     __syncthreads();
+    // codes (and everything else below) may come from the preceding kernel:
+    // wait for it to finish (a no-op unless launched as a dependent)
+    pdl_wait();
     const uint32_t klane = (uint32_t)((lane % a.k_copies) * EK);
     const uint32_t vlane = (FAST ? 128u : 0u) + (uint32_t)((lane % a.v_copies) * EV);
     const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(ktab) + klane;
@@ -546,6 +551,23 @@ decode_kernel(DecArgs a) {
         const int64_t bg = unit / a.n_colblk;
         const int g = (int)(bg % a.H_kv);
         const int b = (int)(bg / a.H_kv);
+        // the segment's first code tiles go to L2 while the queries are prepared
+        const uint8_t *kg = a.kc + bg * a.S_kv * ktb;
+        const uint8_t *vg = a.vc + bg * a.S_kv * vtb;
+        // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
+        const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
+        const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
+        // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
+        const int j_first = (int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile);
+        const int j_last = (int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile);  // exclusive
+        auto prefetch = [&](int j) {
+            if (lane == 0 && j < j_last && j + kStepKeys <= a.S_kv) {
+                prefetch_l2(kg + (int64_t)j * ktb, (uint32_t)(kStepKeys * ktb));
+                prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)(kStepKeys * vtb));
+            }
+        };
+#pragma unroll 1
+        for (int pf = 0; pf < kPrefetchTiles / kStepTiles; ++pf) prefetch(j_first + pf * kStepKeys);
 
         // ---- transformed queries of the unit's columns: q~ = Hn (q (.) s_g^-1)
         __syncwarp();
@@ -612,22 +634,6 @@ decode_kernel(DecArgs a) {
         for (int mt = 0; mt < MT; ++mt)
             us.acc_o[mt][0] = us.acc_o[mt][1] = us.acc_o[mt][2] = us.acc_o[mt][3] = 0.f;
 
-        const uint8_t *kg = a.kc + bg * a.S_kv * ktb;
-        const uint8_t *vg = a.vc + bg * a.S_kv * vtb;
-        // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
-        const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
-        const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
-        // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
-        const int j_first = (int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile);
-        const int j_last = (int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile);  // exclusive
-        auto prefetch = [&](int j) {
-            if (lane == 0 && j < j_last && j + kStepKeys <= a.S_kv) {
-                prefetch_l2(kg + (int64_t)j * ktb, (uint32_t)(kStepKeys * ktb));
-                prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)(kStepKeys * vtb));
-            }
-        };
-#pragma unroll 1
-        for (int pf = 0; pf < kPrefetchTiles / kStepTiles; ++pf) prefetch(j_first + pf * kStepKeys);
 
         // ---- stream the segment, codes double-buffered in registers
         // (a step may run past j_last by one tile; those keys belong to the
@@ -702,6 +708,7 @@ combine_kernel(DecArgs a, __half *__restrict__ out) {
     __shared__ float fac[kMaxRecords];
     __shared__ float red[kCombThreads / 32];
     __shared__ float part[kGroups][kCombDims];
+    pdl_wait();   // the records come from the decode grid
     const int64_t unit = blockIdx.x;
     const int col = blockIdx.y;
     const int cblk = (int)(unit % a.n_colblk);
@@ -822,8 +829,7 @@ cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tb.bytes);
     if (err != cudaSuccess) return err;
-    kern<<<grid, warps_for(D) * 32, tb.bytes, stream>>>(da);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(warps_for(D) * 32), tb.bytes, stream, da);
 }
 
 template <int D>
@@ -978,13 +984,13 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     const int cols = min(kCols, da.G * da.S_q);   // real columns of a column block
     dim3 cgrid((unsigned)units, (unsigned)cols, (unsigned)(a.D / kCombDims));
     __half *out = reinterpret_cast<__half *>(a.out_f16);
+    const dim3 cblock(kCombThreads);
     switch (a.D) {
-        case 32: combine_kernel<32><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
-        case 64: combine_kernel<64><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
-        case 128: combine_kernel<128><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
-        default: combine_kernel<256><<<cgrid, kCombThreads, 0, stream>>>(da, out); break;
+        case 32: return launch_dependent(combine_kernel<32>, cgrid, cblock, 0, stream, da, out);
+        case 64: return launch_dependent(combine_kernel<64>, cgrid, cblock, 0, stream, da, out);
+        case 128: return launch_dependent(combine_kernel<128>, cgrid, cblock, 0, stream, da, out);
+        default: return launch_dependent(combine_kernel<256>, cgrid, cblock, 0, stream, da, out);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace vqkv

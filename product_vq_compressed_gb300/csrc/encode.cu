@@ -80,6 +80,8 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
     extern __shared__ __align__(16) float smem[];
     const int N = p.N, D = p.D;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // a dependent attention launch may be scheduled now (it waits for this grid)
+    pdl_launch_dependents();
     // shared memory: -2c [N][SUBD], |c|^2 [N], max |c|^2, sub-vectors [512][SUBD]
     float *cb_s = smem;
     float *nrm_s = cb_s + ((N * SUBD + 3) & ~3);

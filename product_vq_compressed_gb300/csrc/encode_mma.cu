@@ -238,6 +238,8 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     extern __shared__ __align__(16) float smem[];
     const int N = p.N, D = p.D;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // a dependent attention launch may be scheduled now (it waits for this grid)
+    pdl_launch_dependents();
     const int g = lane >> 2, c4 = lane & 3;
     // shared memory: fp32 codebook [npad][SUBD] (row cslot(n)) | B fragments [n-tile][k-step]
     // [lane] | sub-vectors [512][SUBD] | per-warp A rows [32][AST] | max |c|^2,

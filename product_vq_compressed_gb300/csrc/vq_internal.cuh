@@ -29,6 +29,34 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
     return (__umulhi(f.m, n) + n) >> f.l;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with launch_dependent may start while the preceding
+// kernel on the stream finishes, once every block of that kernel has called
+// pdl_launch_dependents (or exited).  It must call pdl_wait before touching
+// data the preceding kernel writes; pdl_wait returns when that kernel has
+// completed and its memory operations are visible.  Both are no-ops for
+// ordinary launches.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------- registers <-> memory
 // E consecutive elements per lane (E a power of two; naturally aligned).
 
