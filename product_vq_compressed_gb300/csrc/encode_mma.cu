@@ -118,7 +118,7 @@ __device__ __forceinline__ void inverse_token(const EncodeParams &p, int64_t v, 
 // ------------------------------------------------------------ screening operands
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -357,19 +357,38 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             for (int q = 0; q < 4; ++q) { f1[q] = INFINITY; f2[q] = INFINITY; }
             for (int blk = 0; blk < npad / kBlockCols; ++blk) {
                 float bm[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+                // software pipeline over the block's n-tiles: B fragments one
+                // n-tile ahead, minima of n-tile j taken after n-tile j + 1's MMAs
+                constexpr int NTB = kBlockCols / 8;
+                const uint2 *bp = bfrag + (size_t)blk * NTB * C::KS * 32 + lane;
+                uint2 bf[2][C::KS];
+                float acc[2][2][4];
 #pragma unroll
-                for (int j = 0; j < kBlockCols / 8; ++j) {
-                    const int nt = blk * (kBlockCols / 8) + j;
-                    uint2 bf[C::KS];
+                for (int ks = 0; ks < C::KS; ++ks) bf[0][ks] = bp[ks * 32];
 #pragma unroll
-                    for (int ks = 0; ks < C::KS; ++ks) bf[ks] = bfrag[(nt * C::KS + ks) * 32 + lane];
+                for (int j = 0; j <= NTB; ++j) {
+                    if (j < NTB) {
+                        if (j + 1 < NTB) {
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int ks = 0; ks < C::KS; ++ks)
+                                bf[(j + 1) & 1][ks] = bp[((j + 1) * C::KS + ks) * 32];
+                        }
 #pragma unroll
-                        for (int ks = 0; ks < C::KS; ++ks) mma16816(acc, af[mt][ks], bf[ks]);
-                        bm[2 * mt] = min3f(bm[2 * mt], acc[0], acc[1]);
-                        bm[2 * mt + 1] = min3f(bm[2 * mt + 1], acc[2], acc[3]);
+                        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[j & 1][mt][e] = 0.f;
+#pragma unroll
+                            for (int ks = 0; ks < C::KS; ++ks)
+                                mma16816(acc[j & 1][mt], af[mt][ks], bf[j & 1][ks]);
+                        }
+                    }
+                    if (j > 0) {
+                        const int pb = (j - 1) & 1;
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt) {
+                            bm[2 * mt] = min3f(bm[2 * mt], acc[pb][mt][0], acc[pb][mt][1]);
+                            bm[2 * mt + 1] = min3f(bm[2 * mt + 1], acc[pb][mt][2], acc[pb][mt][3]);
+                        }
                     }
                 }
                 const uint32_t tagv = ((uint32_t)blk << 2) | (uint32_t)c4;
