@@ -45,6 +45,7 @@ constexpr int kCols = 8;         // query columns per unit (MMA N)
 constexpr int kTile = 16;        // keys per MMA tile
 constexpr int kPrefetchTiles = 8;  // L2 prefetch distance
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.f;    // base-2 headroom of a column's reference maximum
 
 // ------------------------------------------------------------ primitives
 
@@ -408,16 +409,19 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
         mx0 = fmaxf(mx0, fmaxf(sc4[t][0], sc4[t][2]));
         mx1 = fmaxf(mx1, fmaxf(sc4[t][1], sc4[t][3]));
     }
+    // The reference maximum m of a column moves only when some score exceeds
+    // it by more than kSlack (base 2): then the column's lanes agree on the
+    // new maximum and rescale.  Otherwise p = 2^(s - m) <= 2^kSlack, which
+    // fp16 holds at full relative precision; o / l does not depend on m.
+    if (__any_sync(0xffffffffu, mx0 > u.m0 + kSlack || mx1 > u.m1 + kSlack)) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(u.m0, mx0), mn1 = fmaxf(u.m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    if (__any_sync(0xffffffffu, mn0 != u.m0 || mn1 != u.m1)) {
-        const float al0 = ex2(u.m0 - mu0), al1 = ex2(u.m1 - mu1);
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(u.m0, mx0), mn1 = fmaxf(u.m1, mx1);
+        const float al0 = mn0 == -INFINITY ? 1.f : ex2(u.m0 - mn0);
+        const float al1 = mn1 == -INFINITY ? 1.f : ex2(u.m1 - mn1);
         u.l0 *= al0;
         u.l1 *= al1;
 #pragma unroll
@@ -425,9 +429,11 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
             u.acc_o[mt][0] *= al0; u.acc_o[mt][2] *= al0;
             u.acc_o[mt][1] *= al1; u.acc_o[mt][3] *= al1;
         }
+        u.m0 = mn0;
+        u.m1 = mn1;
     }
-    u.m0 = mn0;
-    u.m1 = mn1;
+    const float mu0 = u.m0 == -INFINITY ? 0.f : u.m0;
+    const float mu1 = u.m1 == -INFINITY ? 0.f : u.m1;
     uint32_t bp[kStepTiles][2];
 #pragma unroll
     for (int t = 0; t < kStepTiles; ++t) {
