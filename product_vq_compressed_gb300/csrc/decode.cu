@@ -44,6 +44,7 @@ __host__ __device__ constexpr int warps_for(int D) { return D >= 256 ? 8 : 12; }
 constexpr int kCols = 8;         // query columns per unit (MMA N)
 constexpr int kTile = 16;        // keys per MMA tile
 constexpr int kPrefetchTiles = 8;  // L2 prefetch distance
+constexpr int kPfKeys = 2 * kTile * 2;  // keys per prefetch: two steps of two tiles
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;    // base-2 headroom of a column's reference maximum
 
@@ -282,14 +283,16 @@ __device__ __forceinline__ void load_step(StepCodes<D, DK, DV> &sc, const uint8_
         else load_codes<SC::NVL>(p, a.vcb, w);
     };
     if (j0 + kStepKeys <= a.S_kv) {
+        // one base address per step; the rows are constant offsets from it
+        const uint8_t *kb = kl + (int64_t)j0 * ktb;
+        const uint8_t *vb = vl + (int64_t)j0 * vtb;
 #pragma unroll
         for (int t = 0; t < kStepTiles; ++t) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                ld_k(kl + (int64_t)(j0 + t * kTile + 8 * r) * ktb, sc.k[t][r]);
+            for (int r = 0; r < 2; ++r) ld_k(kb + (t * kTile + 8 * r) * ktb, sc.k[t][r]);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                ld_v(vl + (int64_t)(j0 + t * kTile + (r & 1) + 8 * (r >> 1)) * vtb, sc.v[t][r]);
+                ld_v(vb + (t * kTile + (r & 1) + 8 * (r >> 1)) * vtb, sc.v[t][r]);
         }
     } else {  // tail of the cache: clamp rows past the last key (masked later)
 #pragma unroll
@@ -566,14 +569,15 @@ decode_kernel(DecArgs a) {
         // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
         const int j_first = (int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile);
         const int j_last = (int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile);  // exclusive
-        auto prefetch = [&](int j) {
-            if (lane == 0 && j < j_last && j + kStepKeys <= a.S_kv) {
-                prefetch_l2(kg + (int64_t)j * ktb, (uint32_t)(kStepKeys * ktb));
-                prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)(kStepKeys * vtb));
+        // L2 prefetch of the keys [j, j + n) (clipped to the segment and the cache)
+        auto prefetch = [&](int j, int n) {
+            const int e = min(min(j + n, j_last), a.S_kv);
+            if (lane == 0 && j < e) {
+                prefetch_l2(kg + (int64_t)j * ktb, (uint32_t)((e - j) * ktb));
+                prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)((e - j) * vtb));
             }
         };
-#pragma unroll 1
-        for (int pf = 0; pf < kPrefetchTiles / kStepTiles; ++pf) prefetch(j_first + pf * kStepKeys);
+        prefetch(j_first, kPrefetchTiles * kTile);
 
         // ---- transformed queries of the unit's columns: q~ = Hn (q (.) s_g^-1)
         __syncwarp();
@@ -655,14 +659,15 @@ decode_kernel(DecArgs a) {
         while (j < j_last) {
             if (j + kStepKeys < j_last)
                 load_step<D, DK, DV, FAST>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
-            prefetch(j + kPrefetchTiles * kTile);
+            // once per two steps (j - j_first is a multiple of 64 here): the
+            // next 64 keys, kPrefetchTiles tiles ahead
+            prefetch(j + kPrefetchTiles * kTile, kPfKeys);
             process_step<D, DK, DV, FAST>(ca, j, us, a, kbase, vbase, krow, vrow, g8, c4,
                                           smem_raw, klane, vlane);
             j += kStepKeys;
             if (j >= j_last) break;
             if (j + kStepKeys < j_last)
                 load_step<D, DK, DV, FAST>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
-            prefetch(j + kPrefetchTiles * kTile);
             process_step<D, DK, DV, FAST>(cb, j, us, a, kbase, vbase, krow, vrow, g8, c4,
                                           smem_raw, klane, vlane);
             j += kStepKeys;
