@@ -115,6 +115,33 @@ VQ_API int vq_encode_values(const void *values_f16, int B, int H, int S, int D,
                      void *stream);
 
 /*
+ * Cache append.  Page: "veloxquant_mlx.cache.vecinfer_cache module",
+ * VecInferKVCache.update_and_fetch (new tokens are encoded and stored after
+ * the ones already cached).  The same encodes as vq_encode_keys and
+ * vq_encode_values, with the codes written into a preallocated cache:
+ *
+ *   codes      [B, H, capacity, D/sub_dim] (output rows offset .. offset+S-1
+ *              of every (b, h); the other rows are not touched).
+ *   capacity   rows per (b, h) of the code buffer.
+ *   offset     first row written: token t of the call goes to row offset + t.
+ *
+ * Everything else (inputs [B, H, S, D], the optional fp16 reconstruction
+ * [B, H, S, D], limits, errors) is as in the calls above; in addition
+ * VQ_ERR_SHAPE when capacity < 0, offset < 0 or offset + S > capacity.
+ * vq_encode_keys(...) equals vq_encode_keys_into(..., capacity = S,
+ * offset = 0, ...).
+ */
+VQ_API int vq_encode_keys_into(const void *keys_f16, int B, int H, int S, int D,
+                               const float *codebook, int n_centroids, int sub_dim,
+                               const float *smooth, int smooth_mode, void *codes,
+                               int code_bytes, int capacity, int offset, void *k_hat_f16,
+                               void *stream);
+VQ_API int vq_encode_values_into(const void *values_f16, int B, int H, int S, int D,
+                                 const float *codebook, int n_centroids, int sub_dim,
+                                 void *codes, int code_bytes, int capacity, int offset,
+                                 void *v_hat_f16, void *stream);
+
+/*
  * Codebook gather.  Page: "Metal Kernels API", section "VecInfer kernels",
  * vecinfer_dequant_metal.
  *
@@ -140,9 +167,17 @@ VQ_API int vq_dequant(const void *codes, int code_bytes, int64_t n_vectors, int 
  * q~ = Hn (q (.) s_g^-1) itself, so that q~ . K~^T equals q . K_hat^T.
  *
  *   q_f16      [B, H_q, S_q, D] fp16, untransformed.
- *   k_codes    [B, H_kv, S_kv, D/k_sub_dim] key codes (k_code_bytes each),
- *              produced by vq_encode_keys with k_codebook and smooth.
- *   v_codes    [B, H_kv, S_kv, D/v_sub_dim] value codes.
+ *   k_codes    [B, H_kv, kv_stride, D/k_sub_dim] key codes (k_code_bytes
+ *              each), produced by vq_encode_keys with k_codebook and smooth;
+ *              rows 0 .. S_kv-1 of every (b, kv head) are the cache.
+ *   v_codes    [B, H_kv, kv_stride, D/v_sub_dim] value codes.
+ *   kv_stride  rows per (b, kv head) of the code buffers (a preallocated
+ *              cache's capacity); 0 means S_kv.  Must be 0 or >= S_kv.
+ *   kv_lens    NULL, or device int32 [B]: batch b holds kv_lens[b] <= S_kv
+ *              cached keys (its rows 0 .. kv_lens[b]-1); its queries align
+ *              to that length (q_abs = kv_lens[b] - S_q + i).  Values are
+ *              clamped to [0, S_kv] on the device; a query with no visible
+ *              key gets a zero row.  NULL: every batch holds S_kv keys.
  *   smooth     key smooth factors, as in vq_encode_keys.
  *   scale      softmax scale (typically 1/sqrt(D)).
  *   causal     != 0: queries align to the tail of the cache, row i sits at
@@ -174,6 +209,8 @@ typedef struct {
     void *out_f16;
     void *workspace;
     size_t workspace_bytes;
+    int kv_stride;
+    const int32_t *kv_lens;
 } vq_attend_args;
 
 /*
@@ -190,7 +227,8 @@ VQ_API size_t vq_attend_workspace_bytes(const vq_attend_args *args);
  *
  * Errors: VQ_ERR_NULL, VQ_ERR_SHAPE (negative sizes, H_kv == 0 or
  * H_q % H_kv != 0, D % sub_dim != 0, S_q > S_kv when causal or windowed,
- * S_kv == 0 with S_q > 0, negative window, bad smooth_mode or code width),
+ * S_kv == 0 with S_q > 0, negative window, bad smooth_mode or code width,
+ * kv_stride < 0 or 0 < kv_stride < S_kv),
  * VQ_ERR_UNSUPPORTED (D not a power of two in [32, 256], sub_dim not in
  * {2, 4, 8}, codebooks over the on-chip limit, n_centroids above the code
  * width), VQ_ERR_ALIGN, VQ_ERR_WORKSPACE, VQ_ERR_CUDA.

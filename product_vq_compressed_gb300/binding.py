@@ -27,6 +27,7 @@ VQ_ERR_WORKSPACE = -5
 VQ_ERR_CUDA = -6
 
 EXPORTED = ("vq_status_str", "vq_encode_keys", "vq_encode_values",
+            "vq_encode_keys_into", "vq_encode_values_into",
             "vq_dequant", "vq_attend_workspace_bytes", "vq_decode_attend",
             "vq_prefill_attend", "vq_decode_attend_noalloc")
 
@@ -55,6 +56,7 @@ class AttendArgs(ctypes.Structure):
         ("sliding_window", ctypes.c_int),
         ("out_f16", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("kv_stride", ctypes.c_int), ("kv_lens", ctypes.c_void_p),
     ]
 
 
@@ -82,13 +84,18 @@ def lib():
                                      i32, vp, i32, vp, vp]
         L.vq_encode_values.argtypes = [vp, i32, i32, i32, i32, vp, i32, i32,
                                        vp, i32, vp, vp]
+        L.vq_encode_keys_into.argtypes = [vp, i32, i32, i32, i32, vp, i32, i32, vp,
+                                          i32, vp, i32, i32, i32, vp, vp]
+        L.vq_encode_values_into.argtypes = [vp, i32, i32, i32, i32, vp, i32, i32,
+                                            vp, i32, i32, i32, vp, vp]
         L.vq_dequant.argtypes = [vp, i32, i64, i32, vp, i32, i32, vp, i32, vp]
         L.vq_attend_workspace_bytes.argtypes = [ctypes.POINTER(AttendArgs)]
         L.vq_attend_workspace_bytes.restype = ctypes.c_size_t
         L.vq_decode_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
         L.vq_prefill_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
         L.vq_decode_attend_noalloc.argtypes = [ctypes.POINTER(AttendArgs), vp]
-        for fn in ("vq_encode_keys", "vq_encode_values", "vq_dequant",
+        for fn in ("vq_encode_keys", "vq_encode_values", "vq_encode_keys_into",
+                   "vq_encode_values_into", "vq_dequant",
                    "vq_decode_attend", "vq_prefill_attend",
                    "vq_decode_attend_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
@@ -165,6 +172,39 @@ def encode_values(values: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
     return codes, v_hat
 
 
+def encode_keys_into(keys: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
+                     smooth: Optional[torch.Tensor], codes: torch.Tensor, offset: int,
+                     k_hat: Optional[torch.Tensor] = None, want_k_hat: bool = False,
+                     stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """vq_encode_keys_into: keys [B, H, S, D] into rows offset .. offset+S-1
+    of the preallocated codes [B, H, capacity, D / sub_dim]."""
+    B, H, S, D = keys.shape
+    if k_hat is None and want_k_hat:
+        k_hat = torch.empty_like(keys)
+    st = lib().vq_encode_keys_into(_ptr(keys), B, H, S, D, _ptr(codebook),
+                                   codebook.shape[0], sub_dim, _ptr(smooth),
+                                   _smooth_mode(smooth), _ptr(codes), _code_bytes(codes),
+                                   codes.shape[2], int(offset), _ptr(k_hat), _stream(stream))
+    _check(st, "vq_encode_keys_into")
+    return codes, k_hat
+
+
+def encode_values_into(values: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
+                       codes: torch.Tensor, offset: int,
+                       v_hat: Optional[torch.Tensor] = None, want_v_hat: bool = False,
+                       stream=None):
+    """vq_encode_values_into: values [B, H, S, D] into rows offset .. of codes."""
+    B, H, S, D = values.shape
+    if v_hat is None and want_v_hat:
+        v_hat = torch.empty_like(values)
+    st = lib().vq_encode_values_into(_ptr(values), B, H, S, D, _ptr(codebook),
+                                     codebook.shape[0], sub_dim, _ptr(codes),
+                                     _code_bytes(codes), codes.shape[2], int(offset),
+                                     _ptr(v_hat), _stream(stream))
+    _check(st, "vq_encode_values_into")
+    return codes, v_hat
+
+
 def dequant(codes: torch.Tensor, codebook: torch.Tensor,
             out: Optional[torch.Tensor] = None, out_f32: bool = True,
             stream=None) -> torch.Tensor:
@@ -185,9 +225,17 @@ def dequant(codes: torch.Tensor, codebook: torch.Tensor,
 
 def make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
                      scale, causal=True, sliding_window=0, out=None,
-                     workspace=None) -> AttendArgs:
+                     workspace=None, s_kv=None, kv_lens=None) -> AttendArgs:
+    """k_codes / v_codes [B, H_kv, rows, n_sub]: the first s_kv rows (all when
+    None) are the cache; kv_lens: optional device int32 [B] per-batch lengths."""
     B, H_q, S_q, D = q.shape
-    _, H_kv, S_kv, _ = k_codes.shape
+    _, H_kv, rows, _ = k_codes.shape
+    if v_codes.shape[2] != rows:
+        raise ValueError("k_codes and v_codes must have the same row count")
+    S_kv = rows if s_kv is None else int(s_kv)
+    if kv_lens is not None and (kv_lens.dtype != torch.int32 or not kv_lens.is_contiguous()
+                                or kv_lens.numel() != B):
+        raise ValueError("kv_lens must be a contiguous int32 tensor of B elements")
     a = AttendArgs()
     a.B, a.H_q, a.H_kv, a.S_q, a.S_kv, a.D = B, H_q, H_kv, S_q, S_kv, D
     a.q_f16 = q.data_ptr()
@@ -207,6 +255,8 @@ def make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
     a.out_f16 = 0 if out is None else out.data_ptr()
     a.workspace = 0 if workspace is None else workspace.data_ptr()
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.kv_stride = rows
+    a.kv_lens = 0 if kv_lens is None else kv_lens.data_ptr()
     return a
 
 
@@ -216,14 +266,14 @@ def attend_workspace_bytes(args: AttendArgs) -> int:
 
 def _attend(fn_name, q, k_codes, k_codebook, v_codes, v_codebook, smooth,
             scale=None, causal=True, sliding_window=0, out=None,
-            workspace=None, stream=None):
+            workspace=None, stream=None, s_kv=None, kv_lens=None):
     D = q.shape[-1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     a = make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
-                         scale, causal, sliding_window, out, workspace)
+                         scale, causal, sliding_window, out, workspace, s_kv, kv_lens)
     if workspace is None:
         need = attend_workspace_bytes(a)
         if need:
@@ -237,17 +287,20 @@ def _attend(fn_name, q, k_codes, k_codebook, v_codes, v_codebook, smooth,
 
 def decode_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
                   scale=None, causal=True, sliding_window=0, out=None,
-                  workspace=None, stream=None) -> torch.Tensor:
-    """vq_decode_attend; raw q [B, H_q, S_q, D] fp16 -> out (same shape)."""
+                  workspace=None, stream=None, s_kv=None, kv_lens=None) -> torch.Tensor:
+    """vq_decode_attend; raw q [B, H_q, S_q, D] fp16 -> out (same shape).
+    s_kv: cached rows of the code buffers (all when None); kv_lens: optional
+    device int32 [B] per-batch lengths."""
     return _attend("vq_decode_attend", q, k_codes, k_codebook, v_codes,
                    v_codebook, smooth, scale, causal, sliding_window, out,
-                   workspace, stream)
+                   workspace, stream, s_kv, kv_lens)
 
 
 def prefill_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
                    scale=None, causal=True, sliding_window=0, out=None,
-                   workspace=None, stream=None) -> torch.Tensor:
-    """vq_prefill_attend (tensor-core path for S_q >= 64)."""
+                   workspace=None, stream=None, s_kv=None, kv_lens=None) -> torch.Tensor:
+    """vq_prefill_attend (tensor-core path for S_q >= 64); s_kv and kv_lens
+    as in decode_attend."""
     return _attend("vq_prefill_attend", q, k_codes, k_codebook, v_codes,
                    v_codebook, smooth, scale, causal, sliding_window, out,
-                   workspace, stream)
+                   workspace, stream, s_kv, kv_lens)

@@ -216,6 +216,8 @@ struct DecArgs {
     float sl;          // scale * log2(e)
     float inv_sqrt_d;
     int causal, window;
+    int64_t stride;        // code rows per (b, kv head)
+    const int32_t *kv_lens;  // keys held by each batch, or null (all S_kv)
     float *ws;         // partial records [nw][slots][kCols][D + 4]
     int n_colblk;
     int tlo, T;        // every unit scans key tiles [tlo, tlo + T)
@@ -561,8 +563,10 @@ decode_kernel(DecArgs a) {
         const int g = (int)(bg % a.H_kv);
         const int b = (int)(bg / a.H_kv);
         // the segment's first code tiles go to L2 while the queries are prepared
-        const uint8_t *kg = a.kc + bg * a.S_kv * ktb;
-        const uint8_t *vg = a.vc + bg * a.S_kv * vtb;
+        const uint8_t *kg = a.kc + bg * a.stride * ktb;
+        const uint8_t *vg = a.vc + bg * a.stride * vtb;
+        // keys held by batch b (clamped to the cache)
+        const int kv_len = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
         // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
         const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
         const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
@@ -604,9 +608,10 @@ decode_kernel(DecArgs a) {
                 reg_fwht<E>(f, lane);
                 store_halves<E>(ws.qt[col] + lane * E, f);
                 if (lane == 0) {
-                    const int q_abs = a.S_kv - a.S_q + i;
-                    int hi = a.causal ? q_abs : a.S_kv - 1;
-                    if (hi > a.S_kv - 1) hi = a.S_kv - 1;
+                    const int L = kv_len;
+                    const int q_abs = L - a.S_q + i;
+                    int hi = a.causal ? q_abs : L - 1;
+                    if (hi > L - 1) hi = L - 1;
                     int lo = a.window > 0 ? q_abs - a.window + 1 : 0;
                     if (lo < 0) lo = 0;
                     ws.lo[col] = lo;
@@ -868,7 +873,14 @@ bool pair_ok(int D, int dk, int dv) {
 }
 
 // Common key-tile range of every unit: the union of what any query row sees.
+// Per-batch lengths (read on the device) can put a batch's queries anywhere
+// in the cache, so then the range is the whole cache.
 void tile_range(const vq_attend_args &a, int *tlo, int *T) {
+    if (a.kv_lens) {
+        *tlo = 0;
+        *T = a.S_kv > 0 ? (a.S_kv + kTile - 1) / kTile : 1;
+        return;
+    }
     const int q_first = a.S_kv - a.S_q, q_last = a.S_kv - 1;
     int hi = a.causal ? q_last : a.S_kv - 1;
     int lo = a.sliding_window > 0 ? q_first - a.sliding_window + 1 : 0;
@@ -972,6 +984,8 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.inv_sqrt_d = (float)(1.0 / sqrt((double)a.D));
     da.causal = a.causal;
     da.window = a.sliding_window;
+    da.stride = a.kv_stride > 0 ? a.kv_stride : a.S_kv;
+    da.kv_lens = a.kv_lens;
     da.ws = reinterpret_cast<float *>(a.workspace);
     da.n_colblk = plan.n_colblk;
     da.tlo = plan.tile_lo;

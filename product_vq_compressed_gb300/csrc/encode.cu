@@ -104,6 +104,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
     __syncthreads();
 
     const int n_sub = D / SUBD;
+    const int lsub = p.log2D - (SUBD == 1 ? 0 : SUBD == 2 ? 1 : SUBD == 4 ? 2 : SUBD == 8 ? 3 : 4);
     const int tok = kSlots / n_sub;  // tokens per tile (n_sub divides 512)
     const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
     CodeT *codes = reinterpret_cast<CodeT *>(p.codes);
@@ -249,7 +250,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
             for (int r = 0; r < kR; ++r) {
                 const int sl = tid + r * kEncThreads;
                 const int64_t gi = v0 * n_sub + sl;
-                if (gi < lim) codes[gi] = (CodeT)i1[r];
+                if (gi < lim) codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)i1[r];
                 if (p.xhat) {
 #pragma unroll
                     for (int t = 0; t < SUBD; ++t)

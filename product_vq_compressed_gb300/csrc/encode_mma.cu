@@ -303,6 +303,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     const float tag_rel = ldexpf(1.f, tbits - 23);
 
     const int n_sub = D / SUBD;
+    const int lsub = p.log2D - (SUBD == 1 ? 0 : SUBD == 2 ? 1 : SUBD == 4 ? 2 : SUBD == 8 ? 3 : 4);
     const int tok = kSlots / n_sub;   // n_sub divides 512
     const int64_t n_tiles = (p.n_vec + tok - 1) / tok;
     CodeT *codes = reinterpret_cast<CodeT *>(p.codes);
@@ -490,7 +491,7 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             const int mine = __shfl_sync(0xffffffffu, code,
                                          (lane & 7) * 4 + (((lane >> 4) << 1) | ((lane >> 3) & 1)));
             const int64_t gi = v0 * n_sub + R0 + lane;
-            if (gi < lim) codes[gi] = (CodeT)mine;
+            if (gi < lim) codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)mine;
             __syncwarp();
             if (p.xhat) {
 #pragma unroll

@@ -189,6 +189,8 @@ struct PrefillArgs {
     int smooth_mode;
     float qscale;                 // scale * log2(e) / sqrt(D), folded into Q~
     int causal, window;
+    int64_t stride;               // code rows per (b, kv head)
+    const int32_t *kv_lens;       // keys held by each batch, or null (all S_kv)
     __half *out;
 };
 
@@ -290,19 +292,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         }
     }
 
-    // ---- visible keys of this row and of the CTA
-    const int q_abs = a.S_kv - a.S_q + row;
-    int hi = a.causal ? q_abs : a.S_kv - 1;
-    hi = min(hi, a.S_kv - 1);
+    // ---- visible keys of this row and of the CTA (batch b holds L keys)
+    const int L = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
+    const int q_abs = L - a.S_q + row;
+    int hi = a.causal ? q_abs : L - 1;
+    hi = min(hi, L - 1);
     int lo = a.window > 0 ? max(0, q_abs - a.window + 1) : 0;
     if (!row_ok) { lo = 1; hi = 0; }
     const int last_row = min(q0 + kRows, a.S_q) - 1;
-    const int qa_first = a.S_kv - a.S_q + q0, qa_last = a.S_kv - a.S_q + last_row;
+    const int qa_first = L - a.S_q + q0, qa_last = L - a.S_q + last_row;
     const int cta_lo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
-    const int cta_hi = min(a.causal ? qa_last : a.S_kv - 1, a.S_kv - 1);
+    const int cta_hi = min(a.causal ? qa_last : L - 1, L - 1);
     const int all_lo = a.window > 0 ? max(0, qa_last - a.window + 1) : 0;   // seen by every row
-    const int all_hi = min(a.causal ? qa_first : a.S_kv - 1, a.S_kv - 1);
-    const int t_first = cta_lo / kKeys, t_last = cta_hi / kKeys;
+    const int all_hi = min(a.causal ? qa_first : L - 1, L - 1);
+    const int t_first = cta_lo / kKeys;
+    const int t_last = cta_hi < cta_lo ? t_first - 1 : cta_hi / kKeys;   // none: empty range
 
     constexpr int kHalfD = kD / 2, kHalfKeys = kKeys / 2;
     float o[kHalfD];                       // output dims hh*64 .. hh*64+63
@@ -313,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     bool failed = false;
 
     const int64_t bg = (int64_t)b * a.H_kv + g;
-    const uint8_t *kcodes = a.kc + bg * a.S_kv * 32 + hh * 16;
-    const uint8_t *vcodes = a.vc + bg * a.S_kv * 32 + hh * 16;
+    const uint8_t *kcodes = a.kc + bg * a.stride * 32 + hh * 16;
+    const uint8_t *vcodes = a.vc + bg * a.stride * 32 + hh * 16;
 
     // codes of one tile in registers: the 16 codes (dims hh*64 ..) of the
     // tile's key r, K and V side
@@ -537,6 +541,8 @@ cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream) {
     p.qscale = (float)((double)a.scale * 1.4426950408889634 / sqrt((double)kD));
     p.causal = a.causal;
     p.window = a.sliding_window;
+    p.stride = a.kv_stride > 0 ? a.kv_stride : a.S_kv;
+    p.kv_lens = a.kv_lens;
     p.out = reinterpret_cast<__half *>(a.out_f16);
     const size_t smem = prefill_smem_bytes();
     cudaError_t err = cudaFuncSetAttribute(prefill_kernel,

@@ -168,7 +168,18 @@ struct EncodeParams {
     int code_bytes;
     __half *xhat;             // [n_vec, D] or null
     FastDiv div_S, div_H;     // by S and H (head of a token)
+    int cap, off;             // code rows per (b, h) and the first row written
 };
+
+// Code index of sub-vector m of token v: token t of (b, h) goes to row
+// off + t of that (b, h)'s cap rows.
+__device__ __forceinline__ int64_t code_index(const EncodeParams &p, int64_t v, int n_sub,
+                                              int m) {
+    if (p.cap == p.S && p.off == 0) return v * n_sub + m;
+    const int64_t bh = p.n_vec < (int64_t(1) << 31) ? (int64_t)fast_div((uint32_t)v, p.div_S)
+                                                    : v / p.S;
+    return ((bh * p.cap + p.off) + (v - bh * p.S)) * n_sub + m;
+}
 
 // Head of token v of a [B, H, S, D] tensor: (v / S) mod H.
 __device__ __forceinline__ int token_head(const EncodeParams &p, int64_t v) {

@@ -27,10 +27,11 @@ int code_capacity_ok(int n_centroids, int code_bytes) {
 
 int encode_common(const void *x, int B, int H, int S, int D,
                   const float *codebook, int N, int sub_dim, const float *smooth,
-                  int smooth_mode, void *codes, int code_bytes, void *xhat,
-                  int rotate, void *stream) {
+                  int smooth_mode, void *codes, int code_bytes, int capacity, int offset,
+                  void *xhat, int rotate, void *stream) {
     if (smooth_mode < 0 || smooth_mode > 2) return VQ_ERR_SHAPE;
     if (B < 0 || H < 0 || S < 0 || D < 1 || sub_dim < 1) return VQ_ERR_SHAPE;
+    if (capacity < 0 || offset < 0 || (int64_t)offset + S > capacity) return VQ_ERR_SHAPE;
     if (D % sub_dim != 0) return VQ_ERR_SHAPE;
     int rc = code_capacity_ok(N, code_bytes);
     if (rc != VQ_OK) return rc;
@@ -63,6 +64,8 @@ int encode_common(const void *x, int B, int H, int S, int D,
     p.xhat = reinterpret_cast<__half *>(xhat);
     p.div_S = vqkv::make_fastdiv((uint32_t)(S > 0 ? S : 1));
     p.div_H = vqkv::make_fastdiv((uint32_t)(H > 0 ? H : 1));
+    p.cap = capacity;
+    p.off = offset;
     return vqkv::launch_encode(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VQ_OK
                : VQ_ERR_CUDA;
@@ -79,6 +82,7 @@ int attend_validate(const vq_attend_args *a) {
     if (a->D % a->k_sub_dim != 0 || a->D % a->v_sub_dim != 0) return VQ_ERR_SHAPE;
     if (a->smooth_mode < 0 || a->smooth_mode > 2) return VQ_ERR_SHAPE;
     if ((a->causal || a->sliding_window > 0) && a->S_q > a->S_kv) return VQ_ERR_SHAPE;
+    if (a->kv_stride < 0 || (a->kv_stride > 0 && a->kv_stride < a->S_kv)) return VQ_ERR_SHAPE;
     if (a->S_kv == 0 && a->S_q > 0 && a->B > 0 && a->H_q > 0) return VQ_ERR_SHAPE;
     int rc = code_capacity_ok(a->k_n_centroids, a->k_code_bytes);
     if (rc != VQ_OK) return rc;
@@ -145,8 +149,18 @@ int vq_encode_keys(const void *keys_f16, int B, int H, int S, int D,
                    const float *smooth, int smooth_mode, void *codes,
                    int code_bytes, void *k_hat_f16, void *stream) {
     return encode_common(keys_f16, B, H, S, D, codebook, n_centroids, sub_dim,
-                         smooth, smooth_mode, codes, code_bytes, k_hat_f16, 1,
+                         smooth, smooth_mode, codes, code_bytes, S, 0, k_hat_f16, 1,
                          stream);
+}
+
+int vq_encode_keys_into(const void *keys_f16, int B, int H, int S, int D,
+                        const float *codebook, int n_centroids, int sub_dim,
+                        const float *smooth, int smooth_mode, void *codes,
+                        int code_bytes, int capacity, int offset, void *k_hat_f16,
+                        void *stream) {
+    return encode_common(keys_f16, B, H, S, D, codebook, n_centroids, sub_dim,
+                         smooth, smooth_mode, codes, code_bytes, capacity, offset,
+                         k_hat_f16, 1, stream);
 }
 
 int vq_encode_values(const void *values_f16, int B, int H, int S, int D,
@@ -154,7 +168,16 @@ int vq_encode_values(const void *values_f16, int B, int H, int S, int D,
                      void *codes, int code_bytes, void *v_hat_f16,
                      void *stream) {
     return encode_common(values_f16, B, H, S, D, codebook, n_centroids, sub_dim,
-                         nullptr, 0, codes, code_bytes, v_hat_f16, 0, stream);
+                         nullptr, 0, codes, code_bytes, S, 0, v_hat_f16, 0, stream);
+}
+
+int vq_encode_values_into(const void *values_f16, int B, int H, int S, int D,
+                          const float *codebook, int n_centroids, int sub_dim,
+                          void *codes, int code_bytes, int capacity, int offset,
+                          void *v_hat_f16, void *stream) {
+    return encode_common(values_f16, B, H, S, D, codebook, n_centroids, sub_dim,
+                         nullptr, 0, codes, code_bytes, capacity, offset, v_hat_f16, 0,
+                         stream);
 }
 
 int vq_dequant(const void *codes, int code_bytes, int64_t n_vectors, int n_sub,

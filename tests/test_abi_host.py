@@ -87,6 +87,21 @@ def test_encode_argument_errors(L):
                               None) == vq.VQ_ERR_NULL
 
 
+def test_encode_into_argument_errors(L):
+    def f(S=8, cap=16, off=0, values=False):
+        if values:
+            return L.vq_encode_values_into(FAKE, 1, 2, S, 128, FAKE, 256, 4, FAKE, 1,
+                                           cap, off, None, None)
+        return L.vq_encode_keys_into(FAKE, 1, 2, S, 128, FAKE, 256, 4, FAKE, 2, FAKE,
+                                     1, cap, off, None, None)
+    assert f(cap=16, off=9) == vq.VQ_ERR_SHAPE        # 9 + 8 rows > 16
+    assert f(off=-1) == vq.VQ_ERR_SHAPE
+    assert f(cap=-1) == vq.VQ_ERR_SHAPE
+    assert f(cap=7) == vq.VQ_ERR_SHAPE
+    assert f(values=True, cap=10, off=3) == vq.VQ_ERR_SHAPE
+    assert f(S=0, cap=4, off=4) == vq.VQ_OK             # empty: nothing written
+
+
 def test_dequant_argument_errors(L):
     assert L.vq_dequant(None, 1, 4, 32, FAKE, 256, 4, FAKE, 1, None) == vq.VQ_ERR_NULL
     assert L.vq_dequant(None, 1, 0, 32, None, 256, 4, None, 1, None) == vq.VQ_OK
@@ -133,6 +148,8 @@ def test_attend_argument_errors(L, fn):
     assert call(D=512) == vq.VQ_ERR_UNSUPPORTED
     assert call(k_sub_dim=16, v_sub_dim=16) == vq.VQ_ERR_UNSUPPORTED
     assert call(k_n_centroids=65536, k_code_bytes=2) == vq.VQ_ERR_UNSUPPORTED
+    assert call(kv_stride=50) == vq.VQ_ERR_SHAPE     # rows per head < S_kv
+    assert call(kv_stride=-1) == vq.VQ_ERR_SHAPE
     assert call(q_f16=FAKE_MIS) == vq.VQ_ERR_ALIGN
     assert call(workspace=FAKE_MIS) == vq.VQ_ERR_ALIGN
     assert L.vq_attend_workspace_bytes(None) == 0
