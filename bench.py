@@ -45,6 +45,10 @@ METRICS = {
     "gqa-decode": ("decode tokens/s (B=32 Hq=32 Hkv=8 S_kv=32768)", "tokens/s"),
     "bulk-encode": ("key-encode vectors/s ([4,32,8192,128] K+V encode)", "vectors/s"),
     "chunked-prefill": ("prefill tokens/s (S_q=2048, window 4096)", "tokens/s"),
+    "decode-append": ("decode tokens/s (append 1 token's K/V codes into a 8256-row cache + "
+                      "attend over 8192, B=1 H=8 D=128)", "tokens/s"),
+    "gqa-decode-ragged": ("decode tokens/s (B=32 Hq=32 Hkv=8, cache lengths U[16384, 32768])",
+                          "tokens/s"),
 }
 
 
@@ -54,18 +58,18 @@ def units_per_step(name, spec):
     return spec.B * spec.S_q                           # query tokens
 
 
-def algorithmic(name, spec):
+def algorithmic(name, spec, lens=None):
     """(dominant kernel, bound, work per launch, unit) -- the per-unit
     figures are stated with the design notes."""
     if name in ("decode-1seq", "bulk-encode"):
         n_sub = spec.B * spec.H_kv * spec.enc_len * spec.n_k
         flops = 2.0 * spec.k_d * spec.k_N * n_sub     # one multiply-add per dim and candidate
         return "encode", "alu", flops, "TFLOP/s"
-    if name == "gqa-decode":
+    if name in ("gqa-decode", "decode-append", "gqa-decode-ragged"):
         per_tok = spec.n_k * np.dtype(spec.k_code_dtype).itemsize + \
             spec.n_v * np.dtype(spec.v_code_dtype).itemsize
-        byts = spec.B * spec.H_kv * spec.S_kv * per_tok + \
-            2 * spec.B * spec.H_q * spec.S_q * spec.D * 2
+        keys = spec.B * spec.S_kv if lens is None else int(np.sum(lens))
+        byts = spec.H_kv * keys * per_tok + 2 * spec.B * spec.H_q * spec.S_q * spec.D * 2
         return "decode", "hbm", float(byts), "GB/s"
     # chunked prefill: QK^T and PV over each query's visible keys
     vis = min(spec.window, spec.S_kv) if spec.window else spec.S_kv
@@ -208,12 +212,21 @@ class Runner:
             dev["v_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_v),
                                          dtype=vq.code_dtype(s.v_N), device="cuda")
             dev["k_hat"] = torch.empty_like(dev["keys"])
+        if name == "decode-append":
+            # the cache: buffers of `capacity` rows holding S_kv - 1 cached
+            # tokens; each step writes the new token into row S_kv - 1
+            for k in ("k_codes", "v_codes"):
+                buf = torch.zeros((s.B, s.H_kv, s.capacity, dev[k].shape[-1]),
+                                  dtype=dev[k].dtype, device="cuda")
+                buf[:, :, :s.S_kv] = dev[k]
+                dev[k] = buf
         dev["out"] = torch.empty_like(dev["q"])
         if name != "bulk-encode":
             args = vq.make_attend_args(dev["q"], dev["k_codes"], dev["k_codebook"],
                                        dev["v_codes"], dev["v_codebook"],
                                        dev.get("smooth"), s.sm_scale, s.causal,
-                                       s.window, dev["out"])
+                                       s.window, dev["out"], s_kv=s.S_kv,
+                                       kv_lens=dev.get("kv_lens"))
             need = vq.attend_workspace_bytes(args)
             dev["ws"] = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
 
@@ -230,6 +243,18 @@ class Runner:
                              d["v_codebook"], d["smooth"], s.sm_scale, s.causal,
                              s.window, out=d["out"], workspace=d["ws"], stream=st)
             return 3
+        if self.name == "decode-append":
+            vq.encode_keys_into(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
+                                d["k_codes"], s.S_kv - 1, stream=st)
+            vq.encode_values_into(d["values"], d["v_codebook"], s.v_d, d["v_codes"],
+                                  s.S_kv - 1, stream=st)
+            if ev: ev[0].record(st)
+            vq.decode_attend(d["q"], d["k_codes"], d["k_codebook"], d["v_codes"],
+                             d["v_codebook"], d["smooth"], s.sm_scale, s.causal,
+                             s.window, out=d["out"], workspace=d["ws"], stream=st,
+                             s_kv=s.S_kv)
+            if ev: ev[1].record(st)
+            return 4
         if self.name == "bulk-encode":
             if ev: ev[0].record(st)
             vq.encode_keys(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
@@ -242,7 +267,7 @@ class Runner:
         if ev: ev[0].record(st)
         fn(d["q"], d["k_codes"], d["k_codebook"], d["v_codes"], d["v_codebook"],
            d["smooth"], s.sm_scale, s.causal, s.window, out=d["out"],
-           workspace=d["ws"], stream=st)
+           workspace=d["ws"], stream=st, kv_lens=d.get("kv_lens"))
         if ev: ev[1].record(st)
         return 2
 
@@ -299,9 +324,9 @@ def run_gpu(args, name, rank, world):
 
     # ---- end to end from pinned host buffers (same C-ABI calls)
     e2e = None
-    if name in ("decode-1seq", "gqa-decode", "chunked-prefill", "bulk-encode"):
-        in_keys = ["keys", "q"] if name == "decode-1seq" else (
-            ["keys", "values"] if name == "bulk-encode" else ["q"])
+    if name in METRICS:
+        in_keys = {"decode-1seq": ["keys", "q"], "bulk-encode": ["keys", "values"],
+                   "decode-append": ["keys", "values", "q"]}.get(name, ["q"])
         host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
                 for k in in_keys}
         out_name = "k_codes" if name == "bulk-encode" else "out"
@@ -331,7 +356,7 @@ def run_gpu(args, name, rank, world):
                "unit": METRICS[name][1], "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
-    kernel, bound, work, wunit = algorithmic(name, spec)
+    kernel, bound, work, wunit = algorithmic(name, spec, inp.get("kv_lens"))
     peaks, peak_src = load_peaks()
     peak, punit = peak_for(bound, peaks)
     dom_s = statistics.mean(dom_ms) / 1e3
@@ -419,10 +444,21 @@ def cpu_baseline(name, spec, inp, budget_s=15.0):
             value = n_total / full
     else:
         per_head, per_row = attend_model()
-        full = n_bg * per_head + n_rows * per_row
-        value = spec.B * spec.S_q / full
+        # per-batch cache lengths: both costs scale with the keys attended
+        frac = float(np.mean(inp["kv_lens"])) / spec.S_kv if "kv_lens" in inp else 1.0
+        full = (n_bg * per_head + n_rows * per_row) * frac
         sample = (f"oracle attention of 1 and 5 rows of one (batch, kv head) over "
                   f"{spec.S_kv} keys, scaled to {n_bg} pairs and {n_rows} rows")
+        if frac != 1.0:
+            sample += f" and by the mean cache length ({frac:.3f} of S_kv)"
+        if name == "decode-append":
+            n_new = spec.B * spec.H_kv * spec.enc_len
+            full += time_encode(n_new)
+            t0 = time.perf_counter()
+            oracle.encode(inp["values"].reshape(-1, D), inp["v_codebook"], rotate=False)
+            full += time.perf_counter() - t0
+            sample = f"oracle key and value encode of the {n_new} new vectors; " + sample
+        value = spec.B * spec.S_q / full
     return {"value": value, "unit": METRICS[name][1], "cores": 1, "kind": "oracle",
             "sample": sample, "est_step_s": full}
 

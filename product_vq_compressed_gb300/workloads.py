@@ -19,10 +19,18 @@ Named workloads (sizes from the documented configurations):
 ``chunked-prefill`` B=1, H_q=32, H_kv=8, D=128, S_q=2048 queries after 16384
                     cached tokens (cache holds 18432 coded tokens), sliding
                     window 4096, causal; uniform uint8 codes; seed 4
+``decode-append``   one decode step of B=1, H_q=H_kv=8, D=128: the new token's
+                    key and value are encoded into row 8191 of a cache of
+                    capacity 8256 rows, then one query per head attends over
+                    the 8192 cached tokens; uniform uint8 codes for the
+                    cache; seed 5
+``gqa-decode-ragged`` gqa-decode with per-sequence cache lengths drawn
+                    uniformly in [S_kv / 2, S_kv]; seed 6
 ==================  =========================================================
 
 Draw order (only what a workload uses): keys, values, outlier channels,
-smooth, key codebook, value codebook, q, key codes, value codes.
+smooth, key codebook, value codebook, q, key codes, value codes, per-batch
+cache lengths.
 Values: fp16 from N(0,1) (drawn in float32, cast to fp16 after any outlier
 scaling); smooth: float32 uniform[0.5, 2] per (KV head, channel); codebooks:
 float32 N(0,1); codes: uniform integers in [0, N).
@@ -64,6 +72,8 @@ class Spec:
     key_outliers: Sequence[int] = ()   # fixed outlier channels (keys)
     outlier_scale: float = 1.0
     outlier_frac: float = 0.0     # fraction of channels drawn as outliers
+    capacity: Optional[int] = None  # rows per (b, kv head) of the code buffers
+    ragged: bool = False          # per-batch cache lengths in [S_kv / 2, S_kv]
 
     @property
     def G(self) -> int:
@@ -109,6 +119,11 @@ WORKLOADS = {
                             S_kv=16384 + 2048, S_q=2048, window=4096, seed=4,
                             draw_keys=False, draw_values=False,
                             draw_codes=True),
+    "decode-append": Spec("decode-append", B=1, H_q=8, H_kv=8, D=128, S_kv=8192,
+                          S_enc=1, capacity=8192 + 64, seed=5, draw_codes=True),
+    "gqa-decode-ragged": Spec("gqa-decode-ragged", B=32, H_q=32, H_kv=8, D=128,
+                              S_kv=32768, seed=6, draw_keys=False,
+                              draw_values=False, draw_codes=True, ragged=True),
 }
 
 
@@ -169,6 +184,8 @@ def make_inputs(spec: Spec) -> dict:
                                       dtype=spec.k_code_dtype)
         out["v_codes"] = rng.integers(0, spec.v_N, size=(spec.B, spec.H_kv, spec.S_kv, spec.n_v),
                                       dtype=spec.v_code_dtype)
+    if spec.ragged:
+        out["kv_lens"] = rng.integers(spec.S_kv // 2, spec.S_kv + 1, size=spec.B).astype(np.int32)
     return out
 
 
