@@ -571,8 +571,15 @@ decode_kernel(DecArgs a) {
         const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
         const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
         // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
-        const int j_first = (int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile);
-        const int j_last = (int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile);  // exclusive
+        // clipped to the keys some query row of batch b can see,
+        // [max(0, L - S_q - W + 1), L - 1] (no lower bound without a window),
+        // so ragged caches read no codes past a batch's length
+        const int vis_lo = a.window > 0 ? max(0, kv_len - a.S_q - a.window + 1) : 0;
+        const int vis_end = (kv_len + kTile - 1) / kTile * kTile;
+        const int j_first = max((int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile),
+                                vis_lo / kTile * kTile);
+        const int j_last = min((int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile),
+                               vis_end);  // exclusive
         // L2 prefetch of the keys [j, j + n) (clipped to the segment and the cache)
         auto prefetch = [&](int j, int n) {
             const int e = min(min(j + n, j_last), a.S_kv);
@@ -660,7 +667,7 @@ decode_kernel(DecArgs a) {
         us.lo_all = max(us.lo_all, j_first); us.hi_all = min(us.hi_all, j_last - 1);
         SC ca, cb;
         int j = j_first;
-        load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
+        if (j < j_last) load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
         while (j < j_last) {
             if (j + kStepKeys < j_last)
                 load_step<D, DK, DV, FAST>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
