@@ -714,7 +714,60 @@ decode_kernel(DecArgs a) {
 }
 
 // Merge the partial records of every (unit, column) and write fp16.  The
-// records of a unit come from the warps whose shares overlap it.  Block
+// records of a unit come from the warps whose shares overlap it.  One block
+// of D threads per (unit, column); warp w takes output dimensions
+// [32 w, 32 w + 32), one per lane.  Every lane walks the unit's records: the
+// maximum M of their m, then o = sum_k 2^(m_k - M) o_k[d] and
+// l = sum_k 2^(m_k - M) l_k, out = o / l.  No shared memory, no barriers
+// (used when a unit has at most kNarrowRecords records).
+constexpr int kMaxRecords = 2048;   // >= warps of any plan (one CTA per SM)
+constexpr int kNarrowRecords = 16;  // up to this many records per unit: one lane per dimension
+
+template <int D>
+__global__ void __launch_bounds__(D)
+combine_kernel(DecArgs a, __half *__restrict__ out) {
+    pdl_wait();   // the records come from the decode grid
+    const int64_t unit = blockIdx.x;
+    const int col = blockIdx.y;
+    const int cblk = (int)(unit % a.n_colblk);
+    const int64_t bg = unit / a.n_colblk;
+    const int cg = cblk * kCols + col;
+    if (cg >= a.G * a.S_q) return;
+    const int b = (int)(bg / a.H_kv), g = (int)(bg % a.H_kv);
+    const int i = cg / a.G, gam = cg % a.G;
+    const int d = threadIdx.x;
+    const int64_t u0 = unit * a.T;
+    const int64_t w_lo = u0 / a.share;
+    int64_t w_hi = (u0 + a.T - 1) / a.share;
+    if (w_hi > a.nw - 1) w_hi = a.nw - 1;
+    int n_rec = (int)(w_hi - w_lo + 1);
+    if (n_rec > kMaxRecords) n_rec = kMaxRecords;   // not reachable: see kMaxRecords
+    // record of warp w for this unit: slot = unit - (first unit of w)
+    auto rec_of = [&](int k) -> const float * {
+        const int64_t w = w_lo + k;
+        const int64_t s = w * a.share;
+        const int64_t slot = a.share <= a.T ? (s >= u0 ? 0 : 1) : unit - s / a.T;
+        return a.ws + ((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4);
+    };
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int k = 0; k < n_rec; ++k) M = fmaxf(M, rec_of(k)[0]);
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 8
+        for (int k = 0; k < n_rec; ++k) {
+            const float *r = rec_of(k);
+            const float f = exp2f(r[0] - M);
+            l = fmaf(f, r[1], l);
+            o = fmaf(f, r[4 + d], o);
+        }
+        o = l > 0.f ? o / l : 0.f;
+    }
+    const int hq = g * a.G + gam;
+    out[(((int64_t)b * a.H_q + hq) * a.S_q + i) * D + d] = __float2half_rn(o);
+}
+
+// Merge for units with many records (long shares of few units): block
 // (unit, column, chunk of kCombDims output dimensions), 256 threads: the
 // block reduces the records' maxima and sums in parallel and keeps each
 // record's rescale factor in shared memory; then 8 groups of kCombDims
@@ -722,11 +775,10 @@ decode_kernel(DecArgs a) {
 // records with many loads in flight, and the groups' sums are added.
 constexpr int kCombThreads = 256;
 constexpr int kCombDims = 32;
-constexpr int kMaxRecords = 2048;   // >= warps of any plan (one CTA per SM)
 
 template <int D>
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(DecArgs a, __half *__restrict__ out) {
+combine_wide_kernel(DecArgs a, __half *__restrict__ out) {
     constexpr int kGroups = kCombThreads / kCombDims;
     __shared__ float fac[kMaxRecords];
     __shared__ float red[kCombThreads / 32];
@@ -1014,9 +1066,21 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     if (err != cudaSuccess) return err;
     const int64_t units = plan.total / plan.tiles;
     const int cols = min(kCols, da.G * da.S_q);   // real columns of a column block
-    dim3 cgrid((unsigned)units, (unsigned)cols, (unsigned)(a.D / kCombDims));
     __half *out = reinterpret_cast<__half *>(a.out_f16);
-    const dim3 cblock(kCombThreads);
+    // records per unit: at most ceil(T / share) + 1
+    const int64_t recs = (plan.tiles + plan.share - 1) / plan.share + 1;
+    if (recs > kNarrowRecords) {
+        const dim3 cgrid((unsigned)units, (unsigned)cols, (unsigned)(a.D / kCombDims));
+        const dim3 cblock(kCombThreads);
+        switch (a.D) {
+            case 32: return launch_dependent(combine_wide_kernel<32>, cgrid, cblock, 0, stream, da, out);
+            case 64: return launch_dependent(combine_wide_kernel<64>, cgrid, cblock, 0, stream, da, out);
+            case 128: return launch_dependent(combine_wide_kernel<128>, cgrid, cblock, 0, stream, da, out);
+            default: return launch_dependent(combine_wide_kernel<256>, cgrid, cblock, 0, stream, da, out);
+        }
+    }
+    const dim3 cgrid((unsigned)units, (unsigned)cols);
+    const dim3 cblock((unsigned)a.D);
     switch (a.D) {
         case 32: return launch_dependent(combine_kernel<32>, cgrid, cblock, 0, stream, da, out);
         case 64: return launch_dependent(combine_kernel<64>, cgrid, cblock, 0, stream, da, out);
