@@ -349,15 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     auto build_k = [&]() { build_rows(kcw, sK, 0u); };
     auto build_v = [&](uint32_t sVb) { build_rows(vcw, sVb, 128u); };
 
-    // ---- first tile's operands, then the pipelined loop:
-    //   QK(j) on the tensor cores   || codes of tile j+1 loading
+    // ---- first tile's K~, then the pipelined loop:
+    //   QK(j) on the tensor cores   || V_hat(j) rebuilt, codes of tile j+1 loading
     //   softmax(j) -> P
-    //   PV(j) on the tensor cores   || K~(j+1), V_hat(j+1) rebuilt
+    //   PV(j) on the tensor cores   || K~(j+1) rebuilt
     //   O = O * alpha + PV(j)
+    // Each rebuild half runs under one product, and V_hat needs one buffer:
+    // PV(j-1) has completed before V_hat(j) is written.
     if (t_first <= t_last) {
         load_codes(t_first * kKeys);
         build_k();
-        build_v(sV + (uint32_t)(t_first & 1) * kTileBytes);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 
     for (int tile = t_first; tile <= t_last; ++tile) {
         const int j0 = tile * kKeys;
-        const uint32_t sVj = sV + (uint32_t)(tile & 1) * kTileBytes;
+        const uint32_t sVj = sV;
         // ---- S = Q~ K~^T into tensor memory
         if (tid == 0) {
             tc_fence_after();
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             }
             mma_commit(bar_s);
         }
+        build_v(sVj);                 // from this tile's value codes
         if (tile < t_last) load_codes(j0 + kKeys);
         // one thread polls (bounded); the block-wide verdict keeps every
         // thread on the same path
@@ -460,7 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         }
         if (tile < t_last) {
             build_k();
-            build_v(sV + (uint32_t)((tile + 1) & 1) * kTileBytes);
             fence_proxy_async();
         }
         ok = true;
