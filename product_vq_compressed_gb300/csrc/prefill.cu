@@ -21,16 +21,20 @@
 //   * One thread issues tcgen05.mma (kind::f16, M = N = 128, K = 16 per
 //     instruction, fp32 accumulate) into tensor memory and commits to an
 //     mbarrier; every thread reads its row back with tcgen05.ld.
-//   * Online softmax in base 2 per row: a max pass and an exp pass over the
-//     score row in tensor memory; P (fp16) goes to shared memory as the A
+//   * Online softmax in base 2 per row over the score row in tensor memory
+//     (see below); P (fp16) goes to shared memory as the A
 //     operand of the second product; the running output stays in registers
 //     (O = O * alpha + P V_hat per tile).
 //   * Key tiles that no row of the CTA can see are skipped; masks are applied
 //     only on tiles that need them.
-//   * Pipelining: while the tensor cores compute Q~K~^T of tile j, the codes
-//     of tile j+1 load into registers; while they compute P V_hat of tile j,
-//     the threads rebuild K~ and V_hat of tile j+1 (V_hat double buffered).  One thread polls each mbarrier; the others wait at the
-//     block barrier that follows.
+//   * Pipelining: while the tensor cores compute Q~K~^T of tile j, the
+//     threads rebuild V_hat of tile j and load the codes of tile j+1; while
+//     they compute P V_hat of tile j, the threads rebuild K~ of tile j+1.  One
+//     thread polls each mbarrier; the others wait at the block barrier that
+//     follows.
+//   * Softmax keeps a reference maximum per row that moves only when a score
+//     exceeds it by more than 2^8: one pass over the scores in tensor memory,
+//     a second only when the maximum moves.
 // Every mbarrier wait is bounded: if one expires the CTA writes NaN rows,
 // waits (bounded) for its own MMAs once more, frees its tensor memory and
 // exits, so a fault shows up in the output instead of hanging the GPU.
@@ -50,6 +54,7 @@ constexpr uint32_t kTileBytes = kRows * kD * 2;  // one fp16 operand tile, 32 Ki
 constexpr uint32_t kHalfTile = kTileBytes / 2;   // 64-element K half, 16 KiB
 constexpr uint32_t kTabBytes = 256 * 256;        // interleaved K | V replicas
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr float kSlack = 8.f;     // base-2 headroom of a row's reference maximum
 
 // ------------------------------------------------------------------ PTX
 
@@ -196,16 +201,17 @@ struct PrefillArgs {
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat x2 | P | tables | misc
+    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat | P | tables | misc
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t sQ = base, sK = base + kTileBytes, sV = base + 2 * kTileBytes,
-                   sP = base + 4 * kTileBytes, sTab = base + 5 * kTileBytes;
-    unsigned char *tab = gbase + 5 * kTileBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 5 * kTileBytes + kTabBytes);
+                   sP = base + 3 * kTileBytes, sTab = base + 4 * kTileBytes;
+    unsigned char *tab = gbase + 4 * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 4 * kTileBytes + kTabBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     float *red = reinterpret_cast<float *>(bars + 4);   // [2][kRows] row exchange
+    int *flg = reinterpret_cast<int *>(red + 2 * kRows); // [2][kRows] "maximum moves"
     const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
 
     // thread = (row r of the tile, column half hh); warps w and w + 4 share
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 
     // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16
     //      (fp32 codebooks first copied into the P region with coalesced loads)
-    float *stage = reinterpret_cast<float *>(gbase + 4 * kTileBytes);
+    float *stage = reinterpret_cast<float *>(gbase + 3 * kTileBytes);
     for (int i = tid; i < a.Nk * kSub; i += kThreads) stage[i] = a.kcb[i];
     for (int i = tid; i < a.Nv * kSub; i += kThreads) stage[1024 + i] = a.vcb[i];
     __syncthreads();
@@ -392,56 +398,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         ph_s ^= 1;
         tc_fence_after();
 
-        // ---- online softmax of row r over this tile: each half takes 64
-        //      keys; the halves exchange their maxima through shared memory
+        // ---- online softmax of row r over this tile, each half 64 keys.
+        //      The row's reference maximum m moves only when a score exceeds
+        //      it by more than kSlack (base 2).  One pass computes P against
+        //      the current m; if the row's m must move (always on its first
+        //      visible tile), the halves agree on the new maximum through
+        //      shared memory and P is recomputed.  Otherwise P = 2^(s - m) <=
+        //      2^kSlack, which fp16 holds at full relative precision.
         const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
         const int jh = j0 + hh * kHalfKeys;
+        auto p_pass = [&](float base, float &mxv) {
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < kHalfKeys / 32; ++c) {
+                float sv[32];
+                tmem_ld32(t_s + c * 32, sv);
+                if (!full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = jh + c * 32 + i;
+                        sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
+                    }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    mxv = fmaxf(mxv, fmaxf(sv[i], sv[i + 1]));
+                    const float p0 = ex2(sv[i] - base), p1 = ex2(sv[i + 1] - base);
+                    ls += p0 + p1;
+                    pk[i / 2] = pack_h2(p0, p1);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    sts128(sP + sw_off(r, hh * 8 + c * 4 + q), pk[4 * q], pk[4 * q + 1],
+                           pk[4 * q + 2], pk[4 * q + 3]);
+            }
+            return ls;
+        };
         float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kHalfKeys / 32; ++c) {
-            float sv[32];
-            tmem_ld32(t_s + c * 32, sv);
-            if (full) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sv[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = jh + c * 32 + i;
-                    mx = fmaxf(mx, (j >= lo && j <= hi) ? sv[i] : -INFINITY);
-                }
-            }
-        }
+        float lsum = p_pass(m == -INFINITY ? 0.f : m, mx);
         red[hh * kRows + r] = mx;
+        flg[hh * kRows + r] = mx > m + kSlack ? 1 : 0;
         __syncthreads();
-        mx = fmaxf(red[r], red[kRows + r]);
-        const float m_new = fmaxf(m, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2(m - m_use);
-        m = m_new;
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < kHalfKeys / 32; ++c) {
-            float sv[32];
-            tmem_ld32(t_s + c * 32, sv);
-            if (!full) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = jh + c * 32 + i;
-                    sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
-                }
-            }
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = ex2(sv[i] - m_use), p1 = ex2(sv[i + 1] - m_use);
-                lsum += p0 + p1;
-                pk[i / 2] = pack_h2(p0, p1);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                sts128(sP + sw_off(r, hh * 8 + c * 4 + q), pk[4 * q], pk[4 * q + 1],
-                       pk[4 * q + 2], pk[4 * q + 3]);
+        const bool row_moves = (flg[r] | flg[kRows + r]) != 0;
+        float alpha = 1.f;
+        if (__any_sync(0xffffffffu, row_moves)) {   // tcgen05.ld is warp-collective
+            const float m_new = row_moves ? fmaxf(m, fmaxf(red[r], red[kRows + r])) : m;
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            if (row_moves) alpha = ex2(m - m_use);
+            m = m_new;
+            float unused = -INFINITY;
+            lsum = p_pass(m_use, unused);
         }
         l = l * alpha + lsum;
         fence_proxy_async();
@@ -512,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 }
 
 size_t prefill_smem_bytes() {
-    return 5 * (size_t)kTileBytes + kTabBytes + 32 + 2 * kRows * sizeof(float) +
+    return 4 * (size_t)kTileBytes + kTabBytes + 32 + 2 * kRows * (sizeof(float) + sizeof(int)) +
            1024;   // + alignment slack
 }
 
