@@ -507,16 +507,18 @@ decode_kernel(DecArgs a) {
     // ---- fp16 tables replicated per bank group (rows past N are zero)
     if constexpr (FAST) {
         // 256 rows x 16 chunks of 16 bytes (8 key, 8 value); every chunk of a
-        // row half holds 16 / EK (16 / EV) copies of its centroid
-        for (int i = tid; i < 256 * 16; i += kThreads) {
-            const int c = i >> 4, q = i & 15;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (q < 8) {
-                if (c < a.Nk) w = replica_chunk<DK>(a.kcbk + c * DK);
-            } else {
-                if (c < a.Nv) w = replica_chunk<DV>(a.vcbk + c * DV);
+        // row half holds 16 / EK (16 / EV) copies of its centroid.  A thread
+        // owns whole rows: both centroid loads are in flight together, then
+        // the 16 stores.
+        for (int c = tid; c < 256; c += kThreads) {
+            const uint4 wk = c < a.Nk ? replica_chunk<DK>(a.kcbk + c * DK) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 wv = c < a.Nv ? replica_chunk<DV>(a.vcbk + c * DV) : make_uint4(0u, 0u, 0u, 0u);
+            uint4 *row = reinterpret_cast<uint4 *>(ktab + c * kFastRow);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                row[q] = wk;
+                row[8 + q] = wv;
             }
-            *reinterpret_cast<uint4 *>(ktab + c * kFastRow + q * 16) = w;
         }
     } else {
         // fp32 copy (coalesced), then the tables word by word
