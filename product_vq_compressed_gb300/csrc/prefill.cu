@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t sQ = base, sK = base + kTileBytes, sV = base + 2 * kTileBytes,
                    sP = base + 3 * kTileBytes, sTab = base + 4 * kTileBytes;
-    unsigned char *tab = gbase + 4 * kTileBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 4 * kTileBytes + kTabBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     float *red = reinterpret_cast<float *>(bars + 4);   // [2][kRows] row exchange
@@ -236,21 +235,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
 
-    // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16
-    //      (fp32 codebooks first copied into the P region with coalesced loads)
-    float *stage = reinterpret_cast<float *>(gbase + 3 * kTileBytes);
-    for (int i = tid; i < a.Nk * kSub; i += kThreads) stage[i] = a.kcb[i];
-    for (int i = tid; i < a.Nv * kSub; i += kThreads) stage[1024 + i] = a.vcb[i];
-    __syncthreads();
-    for (int i = tid; i < 256 * 64; i += kThreads) {
-        const int c = i >> 6, w = i & 63;            // 64 words per 256-byte row
-        const bool is_v = w >= 32;
-        const int t = (w & 1) * 2;                   // dims (t, t+1) of the centroid
-        const int n = is_v ? a.Nv : a.Nk;
-        const float *cb = stage + (is_v ? 1024 : 0);
-        reinterpret_cast<uint32_t *>(tab)[i] =
-            c < n ? pack_h2(cb[c * kSub + t], cb[c * kSub + t + 1]) : 0u;
+    // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16.
+    //      A thread owns a row: both centroid loads in flight, then 16 stores.
+    //      The barrier publishes the table to the rebuilds of every thread.
+    for (int c = tid; c < 256; c += kThreads) {
+        uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
+        if (c < a.Nk) {
+            const float4 f = *reinterpret_cast<const float4 *>(a.kcb + c * kSub);
+            k0 = pack_h2(f.x, f.y);
+            k1 = pack_h2(f.z, f.w);
+        }
+        if (c < a.Nv) {
+            const float4 f = *reinterpret_cast<const float4 *>(a.vcb + c * kSub);
+            v0 = pack_h2(f.x, f.y);
+            v1 = pack_h2(f.z, f.w);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
+            sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
+        }
     }
+    __syncthreads();
 
     // ---- Q~ row r (fp16, swizzled A operand), by the first column half
     if (hh == 0) {
