@@ -258,35 +258,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
     }
     __syncthreads();
 
-    // ---- Q~ row r (fp16, swizzled A operand), by the first column half
-    if (hh == 0) {
-        float x[kD];
+    // ---- Q~ row r (fp16, swizzled A operand).  Thread (r, hh) transforms
+    //      dims [64 hh, 64 hh + 64) of row r: smooth reciprocals from shared
+    //      memory, butterflies h = 1 .. 32 in registers, then stage h = 64
+    //      pairs the two halves through a transposed exchange in the V_hat /
+    //      P region (unused until the loop): x[i], x[i + 64] -> sum, difference.
+    float *rs = reinterpret_cast<float *>(flg + 2 * kRows);   // [kD] 1 / s_g
+    float *xch = reinterpret_cast<float *>(gbase + 2 * kTileBytes);   // [kD][kRows]
+    if (tid < kD) {
+        const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
+        rs[tid] = a.smooth_mode != 0 ? 1.f / sp[tid] : 1.f;
+    }
+    __syncthreads();
+    {
+        constexpr int kH = kD / 2;
+        float x[kH];
         if (row_ok) {
-            const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD;
-            const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
+            const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD + hh * kH;
 #pragma unroll
-            for (int e = 0; e < kD; e += 8) {
+            for (int e = 0; e < kH; e += 8) {
                 const uint4 raw4 = *reinterpret_cast<const uint4 *>(qp + e);
                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw4);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const float2 f = __half22float2(h2[k]);
-                    x[e + 2 * k] = f.x;
-                    x[e + 2 * k + 1] = f.y;
+                    x[e + 2 * k] = f.x * rs[hh * kH + e + 2 * k];
+                    x[e + 2 * k + 1] = f.y * rs[hh * kH + e + 2 * k + 1];
                 }
-            }
-            if (a.smooth_mode != 0) {
-#pragma unroll
-                for (int e = 0; e < kD; ++e) x[e] = x[e] / sp[e];
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < kD; ++e) x[e] = 0.f;
+            for (int e = 0; e < kH; ++e) x[e] = 0.f;
         }
 #pragma unroll
-        for (int h = 1; h < kD; h <<= 1) {
+        for (int h = 1; h < kH; h <<= 1) {
 #pragma unroll
-            for (int i = 0; i < kD; ++i) {
+            for (int i = 0; i < kH; ++i) {
                 if ((i & h) == 0) {
                     const float u = x[i], v = x[i + h];
                     x[i] = u + v;
@@ -295,9 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
             }
         }
 #pragma unroll
-        for (int ch = 0; ch < kD / 8; ++ch) {
+        for (int e = 0; e < kH; ++e) xch[(hh * kH + e) * kRows + r] = x[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kH; ++e) {
+            const float other = xch[((1 - hh) * kH + e) * kRows + r];
+            x[e] = hh == 0 ? x[e] + other : other - x[e];
+        }
+#pragma unroll
+        for (int ch = 0; ch < kH / 8; ++ch) {
             const float *p = x + ch * 8;
-            sts128(sQ + sw_off(r, ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
+            sts128(sQ + sw_off(r, hh * (kH / 8) + ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
                    pack_h2(p[2] * a.qscale, p[3] * a.qscale),
                    pack_h2(p[4] * a.qscale, p[5] * a.qscale),
                    pack_h2(p[6] * a.qscale, p[7] * a.qscale));
@@ -526,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
 
 size_t prefill_smem_bytes() {
     return 4 * (size_t)kTileBytes + kTabBytes + 32 + 2 * kRows * (sizeof(float) + sizeof(int)) +
+           kD * sizeof(float) +
            1024;   // + alignment slack
 }
 
