@@ -153,6 +153,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -444,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    mxv = fmaxf(mxv, fmaxf(sv[i], sv[i + 1]));
+                    mxv = max3f(mxv, sv[i], sv[i + 1]);
                     const float p0 = ex2(sv[i] - base), p1 = ex2(sv[i + 1] - base);
                     ls += p0 + p1;
                     pk[i / 2] = pack_h2(p0, p1);
@@ -458,23 +464,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
         };
         float mx = -INFINITY;
         float lsum = p_pass(m == -INFINITY ? 0.f : m, mx);
+        const bool half_moves = mx > m + kSlack;
         red[hh * kRows + r] = mx;
-        flg[hh * kRows + r] = mx > m + kSlack ? 1 : 0;
-        __syncthreads();
-        const bool row_moves = (flg[r] | flg[kRows + r]) != 0;
-        float alpha = 1.f;
-        if (__any_sync(0xffffffffu, row_moves)) {   // tcgen05.ld is warp-collective
-            const float m_new = row_moves ? fmaxf(m, fmaxf(red[r], red[kRows + r])) : m;
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            if (row_moves) alpha = ex2(m - m_use);
-            m = m_new;
-            float unused = -INFINITY;
-            lsum = p_pass(m_use, unused);
-        }
-        l = l * alpha + lsum;
+        flg[hh * kRows + r] = half_moves ? 1 : 0;
+        // one barrier publishes P (common case) and tells whether any row of
+        // the CTA must move its maximum
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        float alpha = 1.f;
+        if (__syncthreads_or(half_moves)) {
+            const bool row_moves = (flg[r] | flg[kRows + r]) != 0;
+            if (__any_sync(0xffffffffu, row_moves)) {   // tcgen05.ld is warp-collective
+                const float m_new = row_moves ? fmaxf(m, fmaxf(red[r], red[kRows + r])) : m;
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                if (row_moves) alpha = ex2(m - m_use);
+                m = m_new;
+                float unused = -INFINITY;
+                lsum = p_pass(m_use, unused);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+        }
+        l = l * alpha + lsum;
         // ---- P V_hat into tensor memory, next tile's operands meanwhile
         if (tid == 0) {
             tc_fence_after();
