@@ -18,7 +18,14 @@
  *   - fp16 tensors are IEEE binary16 (passed as void*); codebooks, smooth
  *     factors and fp32 outputs are IEEE binary32.
  *   - Codes are unsigned integers of `code_bytes` bytes each: 1 (uint8,
- *     n_centroids <= 256) or 2 (uint16, n_centroids <= 65536).
+ *     n_centroids <= 256) or 2 (uint16, n_centroids <= 65536); or
+ *     code_bytes = 0: bit-packed rows (page "veloxquant_mlx.cache.
+ *     vecinfer_cache module": (D / sub_dim) * b / 8 bytes per token).  Then
+ *     b = ceil(log2 n_centroids) (at least 1, n_centroids <= 65536) bits per
+ *     code, the D / sub_dim codes of one vector form a little-endian bit
+ *     stream (code m in bits [m b, m b + b)), and every vector's row is padded
+ *     to whole 32-bit words: a "[..., D/sub_dim]" code tensor becomes
+ *     "[..., ceil(D/sub_dim * b / 32)]" words.
  *   - Every pointer must be 16-byte aligned (vectorised 128-bit accesses).
  *   - Checks run in this order: sizes (VQ_ERR_SHAPE), limits
  *     (VQ_ERR_UNSUPPORTED), then -- unless the problem is empty, which

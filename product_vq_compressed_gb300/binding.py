@@ -122,8 +122,23 @@ def code_dtype(n_centroids: int) -> torch.dtype:
     return torch.uint8 if n_centroids <= 256 else torch.uint16
 
 
+def packed_code_bits(n_centroids: int) -> int:
+    """Bits per code of bit-packed codes: 2^bits >= n_centroids, bits >= 1."""
+    b = 1
+    while (1 << b) < n_centroids:
+        b += 1
+    return b
+
+
+def packed_row_words(n_sub: int, n_centroids: int) -> int:
+    """32-bit words per token row of n_sub bit-packed codes."""
+    return (n_sub * packed_code_bits(n_centroids) + 31) // 32
+
+
 def _code_bytes(t: torch.Tensor) -> int:
-    return t.element_size()
+    """1 (uint8 codes), 2 (uint16 codes) or 0: int32 tensors hold bit-packed
+    token rows (code m of a row in bits [m b, m b + b) of its 32-bit words)."""
+    return 0 if t.dtype == torch.int32 else t.element_size()
 
 
 def _smooth_mode(smooth: Optional[torch.Tensor]) -> int:
@@ -132,17 +147,24 @@ def _smooth_mode(smooth: Optional[torch.Tensor]) -> int:
     return 1 if smooth.dim() == 1 else 2
 
 
+def _new_codes(B, H, S, n_sub, N, packed, device):
+    if packed:
+        return torch.empty((B, H, S, packed_row_words(n_sub, N)), dtype=torch.int32,
+                           device=device)
+    return torch.empty((B, H, S, n_sub), dtype=code_dtype(N), device=device)
+
+
 def encode_keys(keys: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
                 smooth: Optional[torch.Tensor] = None,
                 codes: Optional[torch.Tensor] = None,
                 k_hat: Optional[torch.Tensor] = None, want_k_hat: bool = False,
-                stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """vq_encode_keys on keys [B, H, S, D] fp16; returns (codes, k_hat)."""
+                stream=None, packed: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """vq_encode_keys on keys [B, H, S, D] fp16; returns (codes, k_hat).
+    packed: codes as bit-packed int32 token rows."""
     B, H, S, D = keys.shape
     N = codebook.shape[0]
     if codes is None:
-        codes = torch.empty((B, H, S, D // sub_dim), dtype=code_dtype(N),
-                            device=keys.device)
+        codes = _new_codes(B, H, S, D // sub_dim, N, packed, keys.device)
     if k_hat is None and want_k_hat:
         k_hat = torch.empty_like(keys)
     st = lib().vq_encode_keys(_ptr(keys), B, H, S, D, _ptr(codebook), N,
@@ -156,13 +178,12 @@ def encode_keys(keys: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
 def encode_values(values: torch.Tensor, codebook: torch.Tensor, sub_dim: int,
                   codes: Optional[torch.Tensor] = None,
                   v_hat: Optional[torch.Tensor] = None,
-                  want_v_hat: bool = False, stream=None):
+                  want_v_hat: bool = False, stream=None, packed: bool = False):
     """vq_encode_values on values [B, H, S, D] fp16; returns (codes, v_hat)."""
     B, H, S, D = values.shape
     N = codebook.shape[0]
     if codes is None:
-        codes = torch.empty((B, H, S, D // sub_dim), dtype=code_dtype(N),
-                            device=values.device)
+        codes = _new_codes(B, H, S, D // sub_dim, N, packed, values.device)
     if v_hat is None and want_v_hat:
         v_hat = torch.empty_like(values)
     st = lib().vq_encode_values(_ptr(values), B, H, S, D, _ptr(codebook), N,
@@ -207,11 +228,14 @@ def encode_values_into(values: torch.Tensor, codebook: torch.Tensor, sub_dim: in
 
 def dequant(codes: torch.Tensor, codebook: torch.Tensor,
             out: Optional[torch.Tensor] = None, out_f32: bool = True,
-            stream=None) -> torch.Tensor:
-    """vq_dequant: codes [..., n_sub] -> [..., n_sub * sub_dim]."""
+            stream=None, n_sub: Optional[int] = None) -> torch.Tensor:
+    """vq_dequant: codes [..., n_sub] -> [..., n_sub * sub_dim]; packed int32
+    rows [..., words] need n_sub."""
     N, d = codebook.shape
-    n_sub = codes.shape[-1]
-    n_vec = codes.numel() // n_sub if n_sub else 0
+    if n_sub is None:
+        n_sub = codes.shape[-1]
+    # vectors: all leading dimensions (one row of codes, or of packed words, each)
+    n_vec = codes.numel() // codes.shape[-1] if codes.shape[-1] else 0
     if out is None:
         out = torch.empty(codes.shape[:-1] + (n_sub * d,),
                           dtype=torch.float32 if out_f32 else torch.float16,
@@ -240,11 +264,11 @@ def make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
     a.B, a.H_q, a.H_kv, a.S_q, a.S_kv, a.D = B, H_q, H_kv, S_q, S_kv, D
     a.q_f16 = q.data_ptr()
     a.k_codes = k_codes.data_ptr()
-    a.k_code_bytes = k_codes.element_size()
+    a.k_code_bytes = _code_bytes(k_codes)
     a.k_codebook = k_codebook.data_ptr()
     a.k_n_centroids, a.k_sub_dim = k_codebook.shape
     a.v_codes = v_codes.data_ptr()
-    a.v_code_bytes = v_codes.element_size()
+    a.v_code_bytes = _code_bytes(v_codes)
     a.v_codebook = v_codebook.data_ptr()
     a.v_n_centroids, a.v_sub_dim = v_codebook.shape
     a.smooth = 0 if smooth is None else smooth.data_ptr()

@@ -107,14 +107,32 @@ __device__ __forceinline__ void load_bytes(const uint8_t *p, uint32_t *w) {
 
 // n codes of `cb` bytes each starting at p, as 32-bit words (room for 2 bytes
 // per code).
+// Codes of `cb` bytes each (1, 2), or bit-packed rows when cb = -bits: then
+// the run keeps the address of its code row (packed codes are read where
+// they are used; row-relative code index = run0 + i).
 template <int NC>
 __device__ __forceinline__ void load_codes(const uint8_t *p, int cb, uint32_t *w) {
-    if (cb == 1) load_bytes<NC>(p, w);
-    else load_bytes<NC * 2>(p, w);
+    if (cb < 0) {
+        const uint64_t a = reinterpret_cast<uint64_t>(p);
+        w[0] = (uint32_t)a;
+        w[1] = (uint32_t)(a >> 32);
+    } else if (cb == 1) {
+        load_bytes<NC>(p, w);
+    } else {
+        load_bytes<NC * 2>(p, w);
+    }
 }
 
 template <int NC>
-__device__ __forceinline__ uint32_t code_at(const uint32_t *w, int cb, int i) {
+__device__ __forceinline__ uint32_t code_at(const uint32_t *w, int cb, int run0, int i) {
+    if (cb < 0) {
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(
+            (uint64_t)w[0] | ((uint64_t)w[1] << 32));
+        const int bits = -cb, bit = (run0 + i) * bits, wi = bit >> 5, sh = bit & 31;
+        uint64_t x = __ldg(row + wi);
+        if (sh + bits > 32) x |= (uint64_t)__ldg(row + wi + 1) << 32;
+        return (uint32_t)(x >> sh) & ((1u << bits) - 1u);
+    }
     // i is a compile-time constant after unrolling
     return cb == 1 ? ((w[i >> 2] >> ((i & 3) * 8)) & 0xFFu)
                    : ((w[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
@@ -204,7 +222,8 @@ struct DecArgs {
     int B, H_q, H_kv, S_q, S_kv, G;
     const __half *q;
     const uint8_t *kc;
-    int kcb;
+    int kcb;           // code bytes (1, 2) or -bits of packed rows
+    int krowb, vrowb;  // bytes per key / value code row
     const float *kcbk;
     int Nk;
     const uint8_t *vc;
@@ -258,8 +277,9 @@ template <int D, int DK, int DV>
 struct StepCodes {
     static constexpr int NKL = D / (4 * DK);
     static constexpr int NVL = D / (8 * DV);
-    static constexpr int KW = (NKL * 2 + 3) / 4;
-    static constexpr int VW = (NVL * 2 + 3) / 4;
+    // room for 2-byte codes, or for a packed code row's address
+    static constexpr int KW = (NKL * 2 + 3) / 4 > 2 ? (NKL * 2 + 3) / 4 : 2;
+    static constexpr int VW = (NVL * 2 + 3) / 4 > 2 ? (NVL * 2 + 3) / 4 : 2;
     uint32_t k[kStepTiles][2][KW];
     uint32_t v[kStepTiles][4][VW];
 };
@@ -335,11 +355,11 @@ template <int DKV, int NC, bool FAST>
 __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const DecArgs &a,
                                             int cb, int N, uint32_t base, int row,
                                             const unsigned char *tab, uint32_t lane_off,
-                                            uint32_t *w) {
+                                            uint32_t *w, int run0 = 0) {
     if constexpr (FAST) {
         gather_sh<DKV>(row_off(words[u >> 2], u & 3, lane_off), w);
     } else {
-        const uint32_t code = min(code_at<NC>(words, cb, u), (uint32_t)(N - 1));
+        const uint32_t code = min(code_at<NC>(words, cb, run0, u), (uint32_t)(N - 1));
         gather<DKV>(base + code * (uint32_t)row, w);
     }
 }
@@ -373,18 +393,19 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
                 if constexpr (DK == 4) {
                     uint32_t w[2];
                     gather_code<4, SC::NKL, FAST>(sc.k[t][r], ks, a, a.kcb, a.Nk, kbase, krow,
-                                                  tabs, klane, w);
+                                                  tabs, klane, w, c4 * SC::NKL);
                     f[t][r][0] = w[0];
                     f[t][r][1] = w[1];
                 } else if constexpr (DK == 2) {
                     gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks, a, a.kcb, a.Nk, kbase,
-                                                  krow, tabs, klane, &f[t][r][0]);
+                                                  krow, tabs, klane, &f[t][r][0], c4 * SC::NKL);
                     gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks + 1, a, a.kcb, a.Nk, kbase,
-                                                  krow, tabs, klane, &f[t][r][1]);
+                                                  krow, tabs, klane, &f[t][r][1], c4 * SC::NKL);
                 } else {
                     if ((ks & 1) == 0)
                         gather_code<8, SC::NKL, FAST>(sc.k[t][r], ks >> 1, a, a.kcb, a.Nk,
-                                                      kbase, krow, tabs, klane, w8[t][r]);
+                                                      kbase, krow, tabs, klane, w8[t][r],
+                                                      c4 * SC::NKL);
                     f[t][r][0] = w8[t][r][2 * (ks & 1)];
                     f[t][r][1] = w8[t][r][2 * (ks & 1) + 1];
                 }
@@ -459,7 +480,8 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
 #pragma unroll
             for (int uu = 0; uu < SC::NVL; ++uu)
                 gather_code<DV, SC::NVL, FAST>(sc.v[t][r], uu, a, a.vcb, a.Nv, vbase, vrow,
-                                               tabs, vlane, &vw[r][uu * (DV / 2)]);
+                                               tabs, vlane, &vw[r][uu * (DV / 2)],
+                                               g8 * SC::NVL);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const uint32_t a0 = __byte_perm(vw[0][mt], vw[1][mt], 0x5410);
@@ -547,8 +569,8 @@ decode_kernel(DecArgs a) {
     const uint32_t vlane = (FAST ? 128u : 0u) + (uint32_t)((lane % a.v_copies) * EV);
     const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(ktab) + klane;
     const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(smem_raw) + (FAST ? 0u : (uint32_t)(vtab - smem_raw)) + vlane;
-    const int64_t ktb = (int64_t)(D / DK) * a.kcb;   // code bytes per key
-    const int64_t vtb = (int64_t)(D / DV) * a.vcb;
+    const int64_t ktb = a.krowb;   // code bytes per key
+    const int64_t vtb = a.vrowb;
     const int n_cols_total = a.G * a.S_q;
     WarpScratch<D> &ws = scratch[warp];
 
@@ -570,8 +592,9 @@ decode_kernel(DecArgs a) {
         // keys held by batch b (clamped to the cache)
         const int kv_len = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
         // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
-        const uint8_t *kl = kg + (int64_t)g8 * ktb + (int64_t)c4 * SC::NKL * a.kcb;
-        const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (int64_t)g8 * SC::NVL * a.vcb;
+        // (packed rows: the row start; the run's first code index is passed on)
+        const uint8_t *kl = kg + (int64_t)g8 * ktb + (a.kcb > 0 ? (int64_t)c4 * SC::NKL * a.kcb : 0);
+        const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (a.vcb > 0 ? (int64_t)g8 * SC::NVL * a.vcb : 0);
         // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
         // clipped to the keys some query row of batch b can see,
         // [max(0, L - S_q - W + 1), L - 1] (no lower bound without a window),
@@ -956,6 +979,19 @@ constexpr int kMinTilesPerWarp = 4;
 
 }  // namespace
 
+vq_attend_args normalize_code_widths(const vq_attend_args &a) {
+    vq_attend_args n = a;
+    auto fix = [](int &cb, int N, int n_sub) {
+        if (cb != 0 || N < 1 || n_sub < 1) return;
+        const int bits = packed_code_bits(N);
+        if (bits == 8 && (n_sub * 8) % 32 == 0) cb = 1;
+        if (bits == 16 && (n_sub * 16) % 32 == 0) cb = 2;
+    };
+    if (a.k_sub_dim > 0) fix(n.k_code_bytes, a.k_n_centroids, a.D / a.k_sub_dim);
+    if (a.v_sub_dim > 0) fix(n.v_code_bytes, a.v_n_centroids, a.D / a.v_sub_dim);
+    return n;
+}
+
 int decode_supported(const vq_attend_args &a) {
     if (a.D != 32 && a.D != 64 && a.D != 128 && a.D != 256) return VQ_ERR_UNSUPPORTED;
     if (!pair_ok(a.D, a.k_sub_dim, a.v_sub_dim)) return VQ_ERR_UNSUPPORTED;
@@ -1032,11 +1068,15 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.G = a.H_q / a.H_kv;
     da.q = reinterpret_cast<const __half *>(a.q_f16);
     da.kc = reinterpret_cast<const uint8_t *>(a.k_codes);
-    da.kcb = a.k_code_bytes;
+    da.kcb = a.k_code_bytes > 0 ? a.k_code_bytes : -packed_code_bits(a.k_n_centroids);
+    da.krowb = a.k_code_bytes > 0 ? (a.D / a.k_sub_dim) * a.k_code_bytes
+                                  : 4 * packed_row_words(a.D / a.k_sub_dim, -da.kcb);
     da.kcbk = a.k_codebook;
     da.Nk = a.k_n_centroids;
     da.vc = reinterpret_cast<const uint8_t *>(a.v_codes);
-    da.vcb = a.v_code_bytes;
+    da.vcb = a.v_code_bytes > 0 ? a.v_code_bytes : -packed_code_bits(a.v_n_centroids);
+    da.vrowb = a.v_code_bytes > 0 ? (a.D / a.v_sub_dim) * a.v_code_bytes
+                                  : 4 * packed_row_words(a.D / a.v_sub_dim, -da.vcb);
     da.vcbk = a.v_codebook;
     da.Nv = a.v_n_centroids;
     da.smooth = a.smooth;

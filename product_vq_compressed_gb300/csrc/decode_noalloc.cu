@@ -61,7 +61,7 @@ extern "C" {
 int vq_decode_attend_noalloc(const vq_attend_args *args, void *stream) {
     if (!args) return VQ_ERR_NULL;
     // same validation as vq_decode_attend, without the caller's workspace
-    vq_attend_args a = *args;
+    vq_attend_args a = vqkv::normalize_code_widths(*args);
     a.workspace = nullptr;
     a.workspace_bytes = 0;
     if (a.B < 0 || a.H_q < 0 || a.H_kv < 0 || a.S_q < 0 || a.S_kv < 0 || a.D < 1 ||
@@ -70,8 +70,8 @@ int vq_decode_attend_noalloc(const vq_attend_args *args, void *stream) {
         a.D % a.v_sub_dim != 0 || a.smooth_mode < 0 || a.smooth_mode > 2 ||
         ((a.causal || a.sliding_window > 0) && a.S_q > a.S_kv) ||
         (a.S_kv == 0 && a.S_q > 0 && a.B > 0 && a.H_q > 0) ||
-        (a.k_code_bytes != 1 && a.k_code_bytes != 2) ||
-        (a.v_code_bytes != 1 && a.v_code_bytes != 2))
+        a.k_code_bytes < 0 || a.k_code_bytes > 2 || a.v_code_bytes < 0 || a.v_code_bytes > 2 ||
+        a.kv_stride < 0 || (a.kv_stride > 0 && a.kv_stride < a.S_kv))
         return VQ_ERR_SHAPE;
     if (a.k_n_centroids < 1 || a.v_n_centroids < 1 ||
         a.k_n_centroids > (a.k_code_bytes == 1 ? 256 : 65536) ||

@@ -35,6 +35,8 @@
 // compare/select per candidate.
 #include <math.h>
 
+#include <type_traits>
+
 #include "vq_internal.cuh"
 
 namespace vqkv {
@@ -87,6 +89,9 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
     float *nrm_s = cb_s + ((N * SUBD + 3) & ~3);
     float *maxn2_s = nrm_s + ((N + 3) & ~3);
     float *y_s = maxn2_s + 4;
+    // packed codes (CodeT = uint32_t): the tile's token rows, assembled here
+    constexpr bool kPacked = std::is_same<CodeT, uint32_t>::value;
+    uint32_t *ptile = reinterpret_cast<uint32_t *>(y_s + kSlots * SUBD);
 
     if (tid == 0) *maxn2_s = 0.f;
     for (int i = tid; i < N * SUBD; i += kEncThreads) cb_s[i] = -2.0f * p.codebook[i];
@@ -140,6 +145,9 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
             } else {
                 for (int e = lane; e < D; e += 32) yv[e] = 0.f;
             }
+        }
+        if constexpr (kPacked) {
+            for (int i = tid; i < tok * p.row_words; i += kEncThreads) ptile[i] = 0u;
         }
         __syncthreads();
 
@@ -250,7 +258,13 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
             for (int r = 0; r < kR; ++r) {
                 const int sl = tid + r * kEncThreads;
                 const int64_t gi = v0 * n_sub + sl;
-                if (gi < lim) codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)i1[r];
+                if (gi < lim) {
+                    if constexpr (kPacked)
+                        packed_or(ptile + (sl >> lsub) * p.row_words, sl & (n_sub - 1),
+                                  p.code_bits, (uint32_t)i1[r]);
+                    else
+                        codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)i1[r];
+                }
                 if (p.xhat) {
 #pragma unroll
                     for (int t = 0; t < SUBD; ++t)
@@ -259,6 +273,14 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
             }
         }
         __syncthreads();
+        if constexpr (kPacked) {   // the tile's packed token rows -> the cache
+            uint32_t *cw = reinterpret_cast<uint32_t *>(p.codes);
+            for (int i = tid; i < tok * p.row_words; i += kEncThreads) {
+                const int t = i / p.row_words, w = i - t * p.row_words;
+                if (v0 + t < p.n_vec) cw[token_row(p, v0 + t) * p.row_words + w] = ptile[i];
+            }
+            __syncthreads();   // before the next tile clears the rows
+        }
 
         // ---- 3. optional reconstruction s^-1 (.) Hn y_hat -> fp16
         if (p.xhat) {
@@ -296,12 +318,20 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
 
 template <typename CodeT>
 __global__ void dequant_kernel(DequantParams p) {
+    constexpr bool kPacked = std::is_same<CodeT, uint32_t>::value;
     const CodeT *codes = reinterpret_cast<const CodeT *>(p.codes);
     const int64_t total = p.n_vec * p.n_sub;
     const int d = p.sub_dim;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        int c = (int)codes[i];
+        int c;
+        if constexpr (kPacked) {
+            const int64_t v = i / p.n_sub;
+            c = (int)packed_get(reinterpret_cast<const uint32_t *>(p.codes) + v * p.row_words,
+                                (int)(i - v * p.n_sub), p.code_bits);
+        } else {
+            c = (int)codes[i];
+        }
         c = c < p.N ? c : p.N - 1;
         const float *src = p.codebook + (size_t)c * d;
         if (p.out_is_f32) {
@@ -342,6 +372,7 @@ cudaError_t launch_encode_t(const EncodeParams &p, cudaStream_t stream) {
 
 template <int SUBD>
 cudaError_t launch_encode_c(const EncodeParams &p, cudaStream_t s) {
+    if (p.code_bytes == 0) return launch_encode_t<SUBD, uint32_t>(p, s);   // packed rows
     return p.code_bytes == 1 ? launch_encode_t<SUBD, uint8_t>(p, s)
                              : launch_encode_t<SUBD, uint16_t>(p, s);
 }
@@ -351,7 +382,8 @@ cudaError_t launch_encode_c(const EncodeParams &p, cudaStream_t s) {
 size_t encode_smem_bytes(int N, int sub_dim) {
     return sizeof(float) * ((((size_t)N * sub_dim + 3) & ~(size_t)3) +
                             (((size_t)N + 3) & ~(size_t)3) + 4 +
-                            (size_t)kSlots * sub_dim);
+                            (size_t)kSlots * sub_dim) +
+           sizeof(uint32_t) * 768;   // packed token rows of a tile (<= 512 / n_sub x words)
 }
 
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream) {
@@ -377,7 +409,9 @@ cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream) {
     int64_t blocks = (p.n_vec * p.n_sub + threads - 1) / threads;
     if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
     if (blocks < 1) blocks = 1;
-    if (p.code_bytes == 1)
+    if (p.code_bytes == 0)
+        dequant_kernel<uint32_t><<<(unsigned)blocks, threads, 0, stream>>>(p);
+    else if (p.code_bytes == 1)
         dequant_kernel<uint8_t><<<(unsigned)blocks, threads, 0, stream>>>(p);
     else
         dequant_kernel<uint16_t><<<(unsigned)blocks, threads, 0, stream>>>(p);

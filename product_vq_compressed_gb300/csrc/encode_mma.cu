@@ -36,6 +36,8 @@
 // argmin wherever that differs from the exact one, as in encode.cu.
 #include <math.h>
 
+#include <type_traits>
+
 #include "vq_internal.cuh"
 
 namespace vqkv {
@@ -251,6 +253,9 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     uint32_t *ascr = reinterpret_cast<uint32_t *>(y_s + kSlots * SUBD);
     float *misc = reinterpret_cast<float *>(ascr + (kThr / 32) * kPassRows * C::AST);
     int *bad_cb = reinterpret_cast<int *>(misc + 1);
+    // packed codes (CodeT = uint32_t): the tile's token rows, assembled here
+    constexpr bool kPacked = std::is_same<CodeT, uint32_t>::value;
+    uint32_t *ptile = reinterpret_cast<uint32_t *>(misc + 4);
 
     if (tid == 0) { misc[0] = 0.f; *bad_cb = 0; }
     for (int i = tid; i < npad * SUBD; i += kThr)
@@ -322,6 +327,9 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                 case 256: forward_token<8>(p, v0 + t, inv_sqrt_d, lane, yv); break;
                 default: forward_token<16>(p, v0 + t, inv_sqrt_d, lane, yv); break;
             }
+        }
+        if constexpr (kPacked) {
+            for (int i = tid; i < tok * p.row_words; i += kThr) ptile[i] = 0u;
         }
         __syncthreads();
 
@@ -491,7 +499,13 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             const int mine = __shfl_sync(0xffffffffu, code,
                                          (lane & 7) * 4 + (((lane >> 4) << 1) | ((lane >> 3) & 1)));
             const int64_t gi = v0 * n_sub + R0 + lane;
-            if (gi < lim) codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)mine;
+            if (gi < lim) {
+                if constexpr (kPacked)
+                    packed_or(ptile + ((R0 + lane) >> lsub) * p.row_words, (R0 + lane) & (n_sub - 1),
+                              p.code_bits, (uint32_t)mine);
+                else
+                    codes[code_index(p, gi >> lsub, n_sub, (int)(gi & (n_sub - 1)))] = (CodeT)mine;
+            }
             __syncwarp();
             if (p.xhat) {
 #pragma unroll
@@ -500,6 +514,13 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             }
         }
         __syncthreads();
+        if constexpr (kPacked) {   // the tile's packed token rows -> the cache
+            uint32_t *cw = reinterpret_cast<uint32_t *>(p.codes);
+            for (int i = tid; i < tok * p.row_words; i += kThr) {
+                const int t = i / p.row_words, w = i - t * p.row_words;
+                if (v0 + t < p.n_vec) cw[token_row(p, v0 + t) * p.row_words + w] = ptile[i];
+            }
+        }
 
         // ---- 3. optional reconstruction -> fp16
         if (p.xhat) {
@@ -525,7 +546,8 @@ size_t mma_smem_bytes(int npad) {
     using C = Cfg<SUBD>;
     return sizeof(float) * (size_t)npad * SUBD + sizeof(uint2) * (size_t)(npad / 8) * C::KS * 32 +
            sizeof(float) * (size_t)kSlots * SUBD +
-           sizeof(uint32_t) * (size_t)(kThr / 32) * kPassRows * C::AST + 16;
+           sizeof(uint32_t) * (size_t)(kThr / 32) * kPassRows * C::AST + 16 +
+           sizeof(uint32_t) * 768;   // packed token rows of a tile (<= 512 / n_sub x words)
 }
 
 template <int SUBD, typename CodeT>
@@ -556,6 +578,7 @@ cudaError_t launch_t(const EncodeParams &p, cudaStream_t stream) {
 
 template <int SUBD>
 cudaError_t launch_c(const EncodeParams &p, cudaStream_t s) {
+    if (p.code_bytes == 0) return launch_t<SUBD, uint32_t>(p, s);   // packed rows
     return p.code_bytes == 1 ? launch_t<SUBD, uint8_t>(p, s) : launch_t<SUBD, uint16_t>(p, s);
 }
 

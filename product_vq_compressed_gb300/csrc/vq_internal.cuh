@@ -154,6 +154,33 @@ __device__ __forceinline__ void reg_fwht(float (&v)[E], int lane) {
     }
 }
 
+// ---------------------------------------------------------------- packed codes
+// Bit-packed codes (code_bytes == 0 at the boundary): b bits per code with
+// 2^b >= n_centroids (b >= 1), the n_sub codes of a token as a little-endian
+// bit stream (code m in bits [m b, m b + b)), every token row padded to whole
+// 32-bit words.
+inline int packed_code_bits(int n_centroids) {
+    int b = 1;
+    while ((1 << b) < n_centroids) ++b;
+    return b;
+}
+__host__ __device__ inline int packed_row_words(int n_sub, int bits) {
+    return (n_sub * bits + 31) / 32;
+}
+// OR code c into position m of a row of 32-bit words (shared memory).
+__device__ __forceinline__ void packed_or(uint32_t *row, int m, int bits, uint32_t c) {
+    const int bit = m * bits, w = bit >> 5, sh = bit & 31;
+    atomicOr(row + w, c << sh);
+    if (sh + bits > 32) atomicOr(row + w + 1, c >> (32 - sh));
+}
+// Code m of a packed row.
+__device__ __forceinline__ uint32_t packed_get(const uint32_t *row, int m, int bits) {
+    const int bit = m * bits, w = bit >> 5, sh = bit & 31;
+    uint64_t x = row[w];
+    if (sh + bits > 32) x |= (uint64_t)row[w + 1] << 32;
+    return (uint32_t)(x >> sh) & ((1u << bits) - 1u);
+}
+
 // ---------------------------------------------------------------- encode
 struct EncodeParams {
     const __half *x;          // [n_vec, D]
@@ -164,21 +191,26 @@ struct EncodeParams {
     const float *smooth;      // mode 1: [D], mode 2: [H, D], mode 0: null
     int smooth_mode;
     int rotate;               // 1 keys (smooth + Hadamard), 0 values
-    void *codes;              // [n_vec, D/sub_dim], code_bytes each
+    void *codes;              // [n_vec, D/sub_dim], code_bytes each (0: packed rows)
     int code_bytes;
+    int code_bits, row_words; // packed codes: bits per code, words per token row
     __half *xhat;             // [n_vec, D] or null
     FastDiv div_S, div_H;     // by S and H (head of a token)
     int cap, off;             // code rows per (b, h) and the first row written
 };
 
-// Code index of sub-vector m of token v: token t of (b, h) goes to row
-// off + t of that (b, h)'s cap rows.
-__device__ __forceinline__ int64_t code_index(const EncodeParams &p, int64_t v, int n_sub,
-                                              int m) {
-    if (p.cap == p.S && p.off == 0) return v * n_sub + m;
+// Cache row of token v: token t of (b, h) goes to row off + t of that
+// (b, h)'s cap rows.
+__device__ __forceinline__ int64_t token_row(const EncodeParams &p, int64_t v) {
+    if (p.cap == p.S && p.off == 0) return v;
     const int64_t bh = p.n_vec < (int64_t(1) << 31) ? (int64_t)fast_div((uint32_t)v, p.div_S)
                                                     : v / p.S;
-    return ((bh * p.cap + p.off) + (v - bh * p.S)) * n_sub + m;
+    return (bh * p.cap + p.off) + (v - bh * p.S);
+}
+// Code index of sub-vector m of token v.
+__device__ __forceinline__ int64_t code_index(const EncodeParams &p, int64_t v, int n_sub,
+                                              int m) {
+    return token_row(p, v) * n_sub + m;
 }
 
 // Head of token v of a [B, H, S, D] tensor: (v / S) mod H.
@@ -200,7 +232,8 @@ cudaError_t launch_encode_mma(const EncodeParams &p, cudaStream_t stream);
 // ---------------------------------------------------------------- dequant
 struct DequantParams {
     const void *codes;
-    int code_bytes;
+    int code_bytes;           // 1, 2, or 0: packed rows
+    int code_bits, row_words; // packed codes: bits per code, words per row of n_sub codes
     int64_t n_vec;
     int n_sub;
     const float *codebook;
@@ -233,6 +266,9 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
                           cudaStream_t stream);
 size_t decode_smem_bytes(const vq_attend_args &a);
 int decode_supported(const vq_attend_args &a);   // VQ_OK or a status
+// The same arguments with packed rows of 8- or 16-bit codes described as
+// uint8 / uint16 codes (identical bytes), so that they take those paths.
+vq_attend_args normalize_code_widths(const vq_attend_args &a);
 
 int prefill_supported(const vq_attend_args &a);  // VQ_OK or a status
 cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream);

@@ -17,8 +17,9 @@ int ilog2(int v) {
     return r;
 }
 
+// code_bytes: 1 (uint8), 2 (uint16), 0 (bit-packed rows of ceil(log2 N)-bit codes)
 int code_capacity_ok(int n_centroids, int code_bytes) {
-    if (code_bytes != 1 && code_bytes != 2) return VQ_ERR_SHAPE;
+    if (code_bytes != 0 && code_bytes != 1 && code_bytes != 2) return VQ_ERR_SHAPE;
     if (n_centroids < 1) return VQ_ERR_UNSUPPORTED;
     const int64_t cap = code_bytes == 1 ? 256 : 65536;
     if ((int64_t)n_centroids > cap) return VQ_ERR_UNSUPPORTED;
@@ -61,6 +62,8 @@ int encode_common(const void *x, int B, int H, int S, int D,
     p.rotate = rotate;
     p.codes = codes;
     p.code_bytes = code_bytes;
+    p.code_bits = code_bytes == 0 ? vqkv::packed_code_bits(N) : 0;
+    p.row_words = code_bytes == 0 ? vqkv::packed_row_words(D / sub_dim, p.code_bits) : 0;
     p.xhat = reinterpret_cast<__half *>(xhat);
     p.div_S = vqkv::make_fastdiv((uint32_t)(S > 0 ? S : 1));
     p.div_H = vqkv::make_fastdiv((uint32_t)(H > 0 ? H : 1));
@@ -192,6 +195,8 @@ int vq_dequant(const void *codes, int code_bytes, int64_t n_vectors, int n_sub,
     vqkv::DequantParams p{};
     p.codes = codes;
     p.code_bytes = code_bytes;
+    p.code_bits = code_bytes == 0 ? vqkv::packed_code_bits(n_centroids) : 0;
+    p.row_words = code_bytes == 0 ? vqkv::packed_row_words(n_sub, p.code_bits) : 0;
     p.n_vec = n_vectors;
     p.n_sub = n_sub;
     p.codebook = codebook;
@@ -204,9 +209,11 @@ int vq_dequant(const void *codes, int code_bytes, int64_t n_vectors, int n_sub,
                : VQ_ERR_CUDA;
 }
 
-size_t vq_attend_workspace_bytes(const vq_attend_args *a) {
+size_t vq_attend_workspace_bytes(const vq_attend_args *args) {
     // Sized for the split-KV path, which both entry points may take.
-    if (!a) return 0;
+    if (!args) return 0;
+    const vq_attend_args n = vqkv::normalize_code_widths(*args);
+    const vq_attend_args *a = &n;
     if (a->H_kv <= 0 || a->H_q <= 0 || a->H_q % a->H_kv != 0 || a->D < 1 ||
         a->S_q <= 0 || a->B <= 0 || a->S_kv <= 0 || a->k_sub_dim < 1 ||
         a->v_sub_dim < 1 || vqkv::decode_supported(*a) != VQ_OK)
@@ -217,10 +224,15 @@ size_t vq_attend_workspace_bytes(const vq_attend_args *a) {
 }
 
 int vq_decode_attend(const vq_attend_args *args, void *stream) {
-    return decode_impl(args, stream);
+    if (!args) return VQ_ERR_NULL;
+    const vq_attend_args n = vqkv::normalize_code_widths(*args);
+    return decode_impl(&n, stream);
 }
 
-int vq_prefill_attend(const vq_attend_args *args, void *stream) {
+int vq_prefill_attend(const vq_attend_args *in, void *stream) {
+    if (!in) return VQ_ERR_NULL;
+    const vq_attend_args n = vqkv::normalize_code_widths(*in);
+    const vq_attend_args *args = &n;
     int rc = attend_validate(args);
     if (rc != VQ_OK) return rc;
     if (vqkv::prefill_supported(*args) != VQ_OK) return decode_impl(args, stream);
