@@ -5,7 +5,8 @@ B=1, H=8, D=128 (uint8 codes, 256x4 codebook) and attend one query per head
 over the 8192 coded keys (values pre-encoded outside the timed region).
 One step = vq_encode_keys + vq_decode_attend (+ its combine pass).
 
-Other workloads (--workload): gqa-decode, bulk-encode, chunked-prefill.
+Other workloads (--workload): gqa-decode, gqa-decode-ragged, decode-append,
+bulk-encode, bulk-encode-packed, chunked-prefill.
 
 Prints ONE JSON line (rank 0).  `value` is device-timed throughput with
 inputs resident in HBM; `e2e` repeats the step through the same C-ABI calls
@@ -44,6 +45,8 @@ METRICS = {
                     "tokens/s"),
     "gqa-decode": ("decode tokens/s (B=32 Hq=32 Hkv=8 S_kv=32768)", "tokens/s"),
     "bulk-encode": ("key-encode vectors/s ([4,32,8192,128] K+V encode)", "vectors/s"),
+    "bulk-encode-packed": ("key-encode vectors/s ([4,32,8192,128] K+V encode, 10-bit packed "
+                           "key codes, 20 B/token-head)", "vectors/s"),
     "chunked-prefill": ("prefill tokens/s (S_q=2048, window 4096)", "tokens/s"),
     "decode-append": ("decode tokens/s (append 1 token's K/V codes into a 8256-row cache + "
                       "attend over 8192, B=1 H=8 D=128)", "tokens/s"),
@@ -53,7 +56,7 @@ METRICS = {
 
 
 def units_per_step(name, spec):
-    if name == "bulk-encode":
+    if name.startswith("bulk-encode"):
         return spec.B * spec.H_kv * spec.enc_len       # key vectors
     return spec.B * spec.S_q                           # query tokens
 
@@ -61,7 +64,7 @@ def units_per_step(name, spec):
 def algorithmic(name, spec, lens=None):
     """(dominant kernel, bound, work per launch, unit) -- the per-unit
     figures are stated with the design notes."""
-    if name in ("decode-1seq", "bulk-encode"):
+    if name in ("decode-1seq", "bulk-encode", "bulk-encode-packed"):
         n_sub = spec.B * spec.H_kv * spec.enc_len * spec.n_k
         flops = 2.0 * spec.k_d * spec.k_N * n_sub     # one multiply-add per dim and candidate
         return "encode", "alu", flops, "TFLOP/s"
@@ -226,9 +229,11 @@ class Runner:
                                                  stream=stream)
             dev["k_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_k),
                                          dtype=vq.code_dtype(s.k_N), device="cuda")
-        if name == "bulk-encode":
-            dev["k_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_k),
-                                         dtype=vq.code_dtype(s.k_N), device="cuda")
+        if name.startswith("bulk-encode"):
+            kw = vq.packed_row_words(s.n_k, s.k_N) if s.packed_keys else s.n_k
+            dev["k_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, kw),
+                                         dtype=torch.int32 if s.packed_keys else
+                                         vq.code_dtype(s.k_N), device="cuda")
             dev["v_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_v),
                                          dtype=vq.code_dtype(s.v_N), device="cuda")
             dev["k_hat"] = torch.empty_like(dev["keys"])
@@ -241,7 +246,7 @@ class Runner:
                 buf[:, :, :s.S_kv] = dev[k]
                 dev[k] = buf
         dev["out"] = torch.empty_like(dev["q"])
-        if name != "bulk-encode":
+        if not name.startswith("bulk-encode"):
             args = vq.make_attend_args(dev["q"], dev["k_codes"], dev["k_codebook"],
                                        dev["v_codes"], dev["v_codebook"],
                                        dev.get("smooth"), s.sm_scale, s.causal,
@@ -275,7 +280,7 @@ class Runner:
                              s_kv=s.S_kv)
             if ev: ev[1].record(st)
             return 4
-        if self.name == "bulk-encode":
+        if self.name.startswith("bulk-encode"):
             if ev: ev[0].record(st)
             vq.encode_keys(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
                            codes=d["k_codes"], k_hat=d["k_hat"], stream=st)
@@ -338,7 +343,7 @@ def run_gpu(args, name, rank, world):
     clk.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
-    out_t = r.d["k_codes"] if name == "bulk-encode" else r.d["out"]
+    out_t = r.d["k_codes"] if name.startswith("bulk-encode") else r.d["out"]
     finite = bool(torch.isfinite(out_t.float()).all()) if out_t.is_floating_point() else True
     if not finite:
         print("warning: non-finite values in the step's output", file=sys.stderr)
@@ -351,10 +356,11 @@ def run_gpu(args, name, rank, world):
     e2e = None
     if name in METRICS:
         in_keys = {"decode-1seq": ["keys", "q"], "bulk-encode": ["keys", "values"],
+                   "bulk-encode-packed": ["keys", "values"],
                    "decode-append": ["keys", "values", "q"]}.get(name, ["q"])
         host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
                 for k in in_keys}
-        out_name = "k_codes" if name == "bulk-encode" else "out"
+        out_name = "k_codes" if name.startswith("bulk-encode") else "out"
         host_out = torch.empty(r.d[out_name].shape, dtype=r.d[out_name].dtype).pin_memory()
         h2d = sum(h.numel() * h.element_size() for h in host.values())
         d2h = host_out.numel() * host_out.element_size()
@@ -453,7 +459,7 @@ def cpu_baseline(name, spec, inp, budget_s=15.0):
 
     n_bg = spec.B * spec.H_kv
     n_rows = spec.B * spec.H_q * spec.S_q
-    if name in ("decode-1seq", "bulk-encode"):
+    if name in ("decode-1seq", "bulk-encode", "bulk-encode-packed"):
         n_total = spec.B * spec.H_kv * spec.enc_len
         per = time_encode(64) / 64
         n_s = int(max(64, min(n_total, 0.6 * budget_s / max(per, 1e-9))))

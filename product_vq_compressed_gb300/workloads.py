@@ -26,6 +26,8 @@ Named workloads (sizes from the documented configurations):
                     cache; seed 5
 ``gqa-decode-ragged`` gqa-decode with per-sequence cache lengths drawn
                     uniformly in [S_kv / 2, S_kv]; seed 6
+``bulk-encode-packed`` bulk-encode with the key codes stored as 10-bit packed
+                    rows (20 bytes per token-head); the same inputs (seed 2)
 ==================  =========================================================
 
 Draw order (only what a workload uses): keys, values, outlier channels,
@@ -73,6 +75,7 @@ class Spec:
     outlier_scale: float = 1.0
     outlier_frac: float = 0.0     # fraction of channels drawn as outliers
     capacity: Optional[int] = None  # rows per (b, kv head) of the code buffers
+    packed_keys: bool = False     # key codes stored as bit-packed rows
     ragged: bool = False          # per-batch cache lengths in [S_kv / 2, S_kv]
 
     @property
@@ -112,6 +115,9 @@ WORKLOADS = {
     "bulk-encode": Spec("bulk-encode", B=4, H_q=32, H_kv=32, D=128, S_kv=8192,
                         k_N=1024, k_d=8, v_N=256, v_d=4, seed=2,
                         outlier_frac=0.02, outlier_scale=10.0),
+    "bulk-encode-packed": Spec("bulk-encode-packed", B=4, H_q=32, H_kv=32, D=128, S_kv=8192,
+                               k_N=1024, k_d=8, v_N=256, v_d=4, seed=2,
+                               outlier_frac=0.02, outlier_scale=10.0, packed_keys=True),
     "gqa-decode": Spec("gqa-decode", B=32, H_q=32, H_kv=8, D=128, S_kv=32768,
                        seed=3, draw_keys=False, draw_values=False,
                        draw_codes=True),
