@@ -557,6 +557,537 @@ size_t prefill_smem_bytes() {
            1024;   // + alignment slack
 }
 
+
+// ------------------------------------------------------------------ two heads per CTA
+//
+// prefill_pair_kernel: one CTA = (batch, two query heads of one KV group,
+// tile of 128 query rows), 416 threads in four roles.  The two heads share
+// the rebuilt K~ and V_hat tiles of their KV head, and the two heads'
+// products and softmaxes interleave so that the tensor cores run one head's
+// product while the CUDA cores run the other head's softmax.
+//   * warps 0-3 / 4-7: softmax of head A / head B; thread = query row r
+//     (tensor-memory lane r), the whole 128-score row of a tile.  P (fp16) is
+//     written back into the first 64 columns of the row's own score columns
+//     and is read from there as the A operand of O += P V_hat.
+//   * warps 8-11: rebuild of K~(j) (one buffer) and V_hat(j) (two buffers)
+//     from the codes, one key row per thread; codes of tile j+1 load ahead.
+//   * warp 12: tensor-memory allocation; one lane issues every tcgen05.mma
+//     in the order S_A(j), S_B(j), then per tile PV_A(j), S_A(j+1), PV_B(j),
+//     S_B(j+1).  A score block is overwritten only after the product that
+//     read its P has completed.
+// Tensor memory (512 columns): S_A | S_B | O_A | O_B.  O stays in tensor
+// memory for the whole key range; when a row's reference maximum moves, the
+// softmax thread rescales its P columns already written in this tile and its
+// O row (the previous P V_hat of that head has completed by then: the score
+// block it waits for was issued after it).
+// Every wait is bounded and also gives up once another role has failed; the
+// verdict is CTA-wide (NaN rows), and the MMA lane drains its products
+// before tensor memory is freed.
+
+constexpr int kPairThreads = 416;
+constexpr int kRebuildWarp = 8;   // first warp of the rebuild role
+constexpr int kMmaWarp = 12;
+constexpr int kPairCols = 512;    // tensor-memory columns
+enum PairBar {
+    kBarSA, kBarSB,       // score block of head A / B complete (commit)
+    kBarOA, kBarOB,       // P V_hat of head A / B complete (commit)
+    kBarPA, kBarPB,       // P of head A / B written (128 arrivals)
+    kBarK,                // K~ written (128 arrivals)
+    kBarV0, kBarV1,       // V_hat buffer 0 / 1 written (128 arrivals)
+    kBarVF0, kBarVF1,     // V_hat buffer 0 / 1 free again (commit)
+    kBarDrain,            // every issued product complete (commit)
+    kNumPairBars
+};
+
+__device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Bounded wait by a whole warp: every lane polls and all leave together.
+// False on timeout (which raises the CTA's failure flag) or once another
+// role has raised it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *fail) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+        if ((it & 255u) == 255u && __any_sync(0xffffffffu, *fail != 0)) return false;
+    }
+    *fail = 1;
+    return false;
+}
+
+// The same for a single thread.
+__device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, volatile int *fail) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 255u) == 255u && *fail != 0) return false;
+    }
+    *fail = 1;
+    return false;
+}
+
+// D (tensor memory) += A (tensor memory, K-major) x B (shared memory).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// 16 consecutive 32-bit columns of this thread's lane, load and store.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+        ::"r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+          "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]),
+          "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+          "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+          "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]),
+          "f"(v[31]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// In-register Walsh-Hadamard butterflies h = 1 .. 32 over 64 values.
+__device__ __forceinline__ void fwht64(float *x) {
+#pragma unroll
+    for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            if ((i & h) == 0) {
+                const float u = x[i], v = x[i + h];
+                x[i] = u + v;
+                x[i + h] = u - v;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte aligned: Q~_A | Q~_B | K~ | V_hat 0 | V_hat 1 | tables | misc
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base, sK = base + 2 * kTileBytes, sV = base + 3 * kTileBytes,
+                   sTab = base + 5 * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 5 * kTileBytes + kTabBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumPairBars);
+    volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *rs = reinterpret_cast<float *>(tmem_slot + 2);   // [kD] 1 / s_g
+    const uint32_t bar0 = smem_u32(bars);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qt = blockIdx.x, b = blockIdx.z;
+    const int hq0 = 2 * blockIdx.y;   // heads hq0 (A) and hq0 + 1 (B): one KV group
+    const int g = hq0 / a.G;
+    const int q0 = qt * kRows;
+
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kPairCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kNumPairBars; ++i) {
+            const bool commit = i == kBarSA || i == kBarSB || i == kBarOA || i == kBarOB ||
+                                i == kBarVF0 || i == kBarVF1 || i == kBarDrain;
+            mbar_init(bar(i), commit ? 1u : 128u);
+        }
+        *fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp >= kRebuildWarp && warp < kMmaWarp) {
+        // smooth reciprocals of the group and the fp16 codebook replicas
+        // (row c = key centroid c x16 | value centroid c x16)
+        const int t = tid - kRebuildWarp * 32;
+        const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
+        rs[t] = a.smooth_mode != 0 ? 1.f / sp[t] : 1.f;
+        for (int c = t; c < 256; c += 128) {
+            uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
+            if (c < a.Nk) {
+                const float4 f = *reinterpret_cast<const float4 *>(a.kcb + c * kSub);
+                k0 = pack_h2(f.x, f.y);
+                k1 = pack_h2(f.z, f.w);
+            }
+            if (c < a.Nv) {
+                const float4 f = *reinterpret_cast<const float4 *>(a.vcb + c * kSub);
+                v0 = pack_h2(f.x, f.y);
+                v1 = pack_h2(f.z, f.w);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
+                sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // ---- key tiles visible to some row of the tile (shared by both heads;
+    //      batch b holds L keys)
+    const int L = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
+    const int last_row = min(q0 + kRows, a.S_q) - 1;
+    const int qa_first = L - a.S_q + q0, qa_last = L - a.S_q + last_row;
+    const int cta_lo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
+    const int cta_hi = min(a.causal ? qa_last : L - 1, L - 1);
+    const int all_lo = a.window > 0 ? max(0, qa_last - a.window + 1) : 0;   // seen by every row
+    const int all_hi = min(a.causal ? qa_first : L - 1, L - 1);
+    const int t_first = cta_lo / kKeys;
+    const int t_last = cta_hi < cta_lo ? t_first - 1 : cta_hi / kKeys;   // none: empty range
+    const int n_tiles = t_last - t_first + 1;
+
+    const int64_t bg = (int64_t)b * a.H_kv + g;
+    const uint8_t *kcodes = a.kc + bg * a.stride * 32;
+    const uint8_t *vcodes = a.vc + bg * a.stride * 32;
+    uint32_t kcw[8], vcw[8];   // rebuild role: the 32 K and V codes of its key row
+    auto load_codes = [&](int j0, int r) {
+        const int j = min(j0 + r, a.S_kv - 1);
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
+        const uint4 d0 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32);
+        const uint4 d1 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32 + 16);
+        kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
+        kcw[4] = c1.x; kcw[5] = c1.y; kcw[6] = c1.z; kcw[7] = c1.w;
+        vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
+        vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
+    };
+
+    if (warp < kRebuildWarp) {
+        // ---- Q~ row r of head h (fp16, swizzled A operand): each half's
+        //      butterflies below 64 in registers, the first half parked in
+        //      the K~ / V_hat region (free until the loop), then the stage
+        //      h = 64 pairs the halves: x[i], x[i + 64] -> sum, difference.
+        const int h = warp >> 2, r = tid & (kRows - 1), row = q0 + r;
+        float *xs = reinterpret_cast<float *>(gbase + 2 * kTileBytes) + h * (kD / 2) * kRows;
+        const __half *qp = a.q + (((int64_t)b * a.H_q + hq0 + h) * a.S_q + row) * kD;
+        float x[kD / 2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (row < a.S_q) {
+#pragma unroll
+                for (int e = 0; e < kD / 2; e += 8) {
+                    const uint4 raw4 = *reinterpret_cast<const uint4 *>(qp + half * 64 + e);
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw4);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = __half22float2(h2[k]);
+                        x[e + 2 * k] = f.x * rs[half * 64 + e + 2 * k];
+                        x[e + 2 * k + 1] = f.y * rs[half * 64 + e + 2 * k + 1];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kD / 2; ++e) x[e] = 0.f;
+            }
+            fwht64(x);
+            if (half == 0) {
+#pragma unroll
+                for (int e = 0; e < kD / 2; ++e) xs[e * kRows + r] = x[e];
+            }
+        }
+        const uint32_t sQh = sQ + (uint32_t)h * kTileBytes;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            float lo8[8], hi8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float u = xs[(ch * 8 + k) * kRows + r], v = x[ch * 8 + k];
+                lo8[k] = (u + v) * a.qscale;
+                hi8[k] = (u - v) * a.qscale;
+            }
+            sts128(sQh + sw_off(r, ch), pack_h2(lo8[0], lo8[1]), pack_h2(lo8[2], lo8[3]),
+                   pack_h2(lo8[4], lo8[5]), pack_h2(lo8[6], lo8[7]));
+            sts128(sQh + sw_off(r, 8 + ch), pack_h2(hi8[0], hi8[1]), pack_h2(hi8[2], hi8[3]),
+                   pack_h2(hi8[4], hi8[5]), pack_h2(hi8[6], hi8[7]));
+        }
+        fence_proxy_async();
+    } else if (warp < kMmaWarp && n_tiles > 0) {
+        load_codes(t_first * kKeys, tid - kRebuildWarp * 32);
+    }
+    __syncthreads();   // Q~ written, the scratch region free
+
+    // softmax role: head h, row r (tensor-memory lane r)
+    const int h = (warp >> 2) & 1, r = tid & (kRows - 1), row = q0 + r;
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lanes + (uint32_t)(h * kKeys);
+    const uint32_t t_o = tmem + lanes + (uint32_t)(2 * kKeys + h * kD);
+    float l = 0.f;
+    if (warp < kRebuildWarp) {
+        // ================= softmax of head h, row r
+        const int q_abs = L - a.S_q + row;
+        int hi = a.causal ? q_abs : L - 1;
+        hi = min(hi, L - 1);
+        int lo = a.window > 0 ? max(0, q_abs - a.window + 1) : 0;
+        if (row >= a.S_q) { lo = 1; hi = 0; }
+        float m = -INFINITY;
+        uint32_t ph = 0;
+        for (int tile = t_first; tile <= t_last; ++tile) {
+            if (!warp_wait(bar(kBarSA + h), ph, fail)) break;
+            ph ^= 1;
+            tc_fence_after();
+            const int j0 = tile * kKeys;
+            const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
+            float alpha_o = 1.f;   // rescale owed by this row's O
+#pragma unroll 1
+            for (int c = 0; c < kKeys / 32; ++c) {
+                float sv[32];
+                tmem_ld32(t_s + c * 32, sv);
+                if (!full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = j0 + c * 32 + i;
+                        sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
+                    }
+                }
+                float cmax = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) cmax = max3f(cmax, sv[i], sv[i + 1]);
+                // the reference maximum moves only past kSlack (base 2)
+                const bool moves = cmax > m + kSlack;
+                if (__any_sync(0xffffffffu, moves)) {
+                    const float alpha = moves ? ex2(m - cmax) : 1.f;   // 0 from -inf
+                    if (moves) {
+                        l *= alpha;
+                        alpha_o *= alpha;
+                        m = cmax;
+                    }
+                    // P columns already written in this tile, rescaled
+                    if (c > 0) tmem_wait_st();
+                    for (int cc = 0; cc < c; ++cc) {
+                        uint32_t pw[16];
+                        tmem_ld16(t_s + cc * 16, pw);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&pw[i]));
+                            pw[i] = pack_h2(f.x * alpha, f.y * alpha);
+                        }
+                        tmem_st16(t_s + cc * 16, pw);
+                    }
+                }
+                const float base_m = m == -INFINITY ? 0.f : m;
+                uint32_t pk[16];
+                float ls = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = ex2(sv[i] - base_m), p1 = ex2(sv[i + 1] - base_m);
+                    ls += p0 + p1;
+                    pk[i / 2] = pack_h2(p0, p1);
+                }
+                l += ls;
+                tmem_st16(t_s + c * 16, pk);
+            }
+            // the row's O (all earlier tiles' P V_hat, complete) follows the
+            // moved maximum; on the first tile the product overwrites O
+            if (tile > t_first && __any_sync(0xffffffffu, alpha_o != 1.f)) {
+#pragma unroll 1
+                for (int c = 0; c < kD / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(t_o + c * 32, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha_o;
+                    tmem_st32(t_o + c * 32, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(kBarPA + h));
+        }
+        __syncwarp();
+    } else if (warp < kMmaWarp) {
+        // ================= rebuild of K~ and V_hat, key row r of each tile
+        const int r = tid - kRebuildWarp * 32;
+        const uint32_t lane_off = (uint32_t)((lane & 15) * 8);
+        auto build_row = [&](const uint32_t *cw, uint32_t dst, uint32_t side) {
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint32_t w = cw[ch >> 1];
+                const uint32_t i0 = (uint32_t)(ch & 1) * 2u;
+                const uint32_t o = side + lane_off;
+                const uint2 e0 = lds64(sTab + __byte_perm(w, o, 0x6504u | (i0 << 4)));
+                const uint2 e1 = lds64(sTab + __byte_perm(w, o, 0x6504u | ((i0 + 1u) << 4)));
+                sts128(dst + sw_off(r, ch), e0.x, e0.y, e1.x, e1.y);
+            }
+        };
+        uint32_t ph_sb = 0, ph_vf = 0;   // ph_vf: bit b = parity of V_hat buffer b
+        for (int tile = t_first; tile <= t_last; ++tile) {
+            const int i = tile - t_first;
+            if (i > 0) {   // both score blocks of the previous tile read K~
+                if (!warp_wait(bar(kBarSB), ph_sb, fail)) break;
+                ph_sb ^= 1;
+            }
+            build_row(kcw, sK, 0u);
+            fence_proxy_async();
+            mbar_arrive(bar(kBarK));
+            const int vb = i & 1;
+            if (i > 1) {   // the products of tile - 2 read this V_hat buffer
+                if (!warp_wait(bar(kBarVF0 + vb), (ph_vf >> vb) & 1u, fail)) break;
+                ph_vf ^= 1u << vb;
+            }
+            build_row(vcw, sV + (uint32_t)vb * kTileBytes, 128u);
+            fence_proxy_async();
+            mbar_arrive(bar(kBarV0 + vb));
+            if (tile < t_last) load_codes((tile + 1) * kKeys, r);
+        }
+        __syncwarp();
+    } else {
+        // ================= tensor-core issue (one lane)
+        if (lane == 0 && n_tiles > 0) {
+            auto issue_s = [&](int hh) {
+                const uint32_t sQh = sQ + (uint32_t)hh * kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
+                    mma_f16(tmem + (uint32_t)(hh * kKeys), smem_desc(sQh + off),
+                            smem_desc(sK + off), kIdesc, ks > 0);
+                }
+                mma_commit(bar(kBarSA + hh));
+            };
+            auto issue_pv = [&](int hh, uint32_t sVb, bool acc) {
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks) {
+                    // A = P: keys 16 ks .. 16 ks + 15 in columns 8 ks .. 8 ks + 7
+                    mma_f16_ta(tmem + (uint32_t)(2 * kKeys + hh * kD),
+                               tmem + (uint32_t)(hh * kKeys + ks * 8),
+                               smem_desc_mn(sVb + (uint32_t)ks * 2048u, kHalfTile), kIdescBmn,
+                               (acc || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(kBarOA + hh));
+            };
+            uint32_t ph_k = 0, ph_v = 0, ph_p[2] = {0u, 0u}, ph_o[2] = {0u, 0u};   // ph_v: bit b per buffer
+            bool ok = lone_wait(bar(kBarK), ph_k, fail);
+            ph_k ^= 1;
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_s(1);
+            }
+            for (int tile = t_first; ok && tile <= t_last; ++tile) {
+                const int i = tile - t_first, vb = i & 1;
+                const uint32_t sVb = sV + (uint32_t)vb * kTileBytes;
+                const bool more = tile < t_last;
+                if (!(ok = lone_wait(bar(kBarV0 + vb), (ph_v >> vb) & 1u, fail))) break;
+                ph_v ^= 1u << vb;
+                if (!(ok = lone_wait(bar(kBarPA), ph_p[0], fail))) break;
+                ph_p[0] ^= 1;
+                tc_fence_after();
+                issue_pv(0, sVb, i > 0);
+                if (more) {
+                    if (!(ok = lone_wait(bar(kBarK), ph_k, fail))) break;
+                    ph_k ^= 1;
+                    if (!(ok = lone_wait(bar(kBarOA), ph_o[0], fail))) break;
+                    ph_o[0] ^= 1;
+                    tc_fence_after();
+                    issue_s(0);
+                }
+                if (!(ok = lone_wait(bar(kBarPB), ph_p[1], fail))) break;
+                ph_p[1] ^= 1;
+                tc_fence_after();
+                issue_pv(1, sVb, i > 0);
+                mma_commit(bar(kBarVF0 + vb));
+                if (more) {
+                    if (!(ok = lone_wait(bar(kBarOB), ph_o[1], fail))) break;
+                    ph_o[1] ^= 1;
+                    tc_fence_after();
+                    issue_s(1);
+                }
+            }
+            // every product issued completes before the output is read and
+            // tensor memory is freed
+            mma_commit(bar(kBarDrain));
+            for (uint32_t it = 0; it < kWaitLimit; ++it) {
+                if (mbar_try(bar(kBarDrain), 0u)) break;
+                if (it + 1 == kWaitLimit) *fail = 1;
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();   // every role has left its loop; every product has completed
+    tc_fence_after();
+
+    if (warp < kRebuildWarp) {
+        // ---- output row r of head h (tcgen05.ld is warp-collective: every
+        //      lane loads, only rows of the query block are stored)
+        const bool failed = *fail != 0;
+        const bool have_o = n_tiles > 0 && !failed;
+        const float inv = failed ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
+        __half *op = a.out + (((int64_t)b * a.H_q + hq0 + h) * a.S_q + row) * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+            float ov[32];
+            if (have_o) {
+                tmem_ld32(t_o + c * 32, ov);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+            }
+            if (row < a.S_q) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const float *p = ov + ch * 8;
+                    uint4 v;
+                    v.x = pack_h2(p[0] * inv, p[1] * inv);
+                    v.y = pack_h2(p[2] * inv, p[3] * inv);
+                    v.z = pack_h2(p[4] * inv, p[5] * inv);
+                    v.w = pack_h2(p[6] * inv, p[7] * inv);
+                    *reinterpret_cast<uint4 *>(op + c * 32 + ch * 8) = v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n"
+                     ::"r"(tmem), "r"(kPairCols));
+    }
+}
+
+size_t prefill_pair_smem_bytes() {
+    return 5 * (size_t)kTileBytes + kTabBytes + kNumPairBars * 8 + 8 + kD * sizeof(float) +
+           1024;   // + alignment slack
+}
+
 }  // namespace
 
 int prefill_supported(const vq_attend_args &a) {
@@ -586,12 +1117,23 @@ cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream) {
     p.stride = a.kv_stride > 0 ? a.kv_stride : a.S_kv;
     p.kv_lens = a.kv_lens;
     p.out = reinterpret_cast<__half *>(a.out_f16);
+    const unsigned q_tiles = (unsigned)((a.S_q + kRows - 1) / kRows);
+    if (p.G % 2 == 0) {   // two query heads of one KV group per CTA
+        const size_t smem = prefill_pair_smem_bytes();
+        cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+        if (err != cudaSuccess) return err;
+        dim3 grid(q_tiles, (unsigned)(a.H_q / 2), (unsigned)a.B);
+        prefill_pair_kernel<<<grid, kPairThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
     const size_t smem = prefill_smem_bytes();
     cudaError_t err = cudaFuncSetAttribute(prefill_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid((unsigned)((a.S_q + kRows - 1) / kRows), (unsigned)a.H_q, (unsigned)a.B);
+    dim3 grid(q_tiles, (unsigned)a.H_q, (unsigned)a.B);
     prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
