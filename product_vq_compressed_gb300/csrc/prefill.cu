@@ -613,6 +613,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded wait by a whole warp: every lane polls and all leave together.
 // False on timeout (which raises the CTA's failure flag) or once another
 // role has raised it.
@@ -625,23 +630,34 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return false;
 }
 
-// The same for a single thread.
-__device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, volatile int *fail) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 255u && *fail != 0) return false;
-    }
-    *fail = 1;
-    return false;
+// Products D (tensor memory) += A x B with A in shared memory (ss) or in
+// tensor memory (ts, K-major) and B in shared memory, and the commit, each
+// issued by one lane of a converged warp (elect.sync): the warp runs the
+// issue loop together, so its operand descriptors stay warp-uniform and a
+// product costs a few instructions.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred e, p;\n .reg .b32 lid;\n"
+        " elect.sync lid|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
-// D (tensor memory) += A (tensor memory, K-major) x B (shared memory).
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        "{\n .reg .pred e, p;\n .reg .b32 lid;\n"
+        " elect.sync lid|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
         ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 lid;\n elect.sync lid|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n"
+        ::"r"(bar) : "memory");
 }
 
 // 16 consecutive 32-bit columns of this thread's lane, load and store.
@@ -727,7 +743,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
         for (int i = 0; i < kNumPairBars; ++i) {
             const bool commit = i == kBarSA || i == kBarSB || i == kBarOA || i == kBarOB ||
                                 i == kBarVF0 || i == kBarVF1 || i == kBarDrain;
-            mbar_init(bar(i), commit ? 1u : 128u);
+            mbar_init(bar(i), commit ? 1u : 4u);
         }
         *fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -929,7 +945,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(kBarPA + h));
+            warp_arrive(bar(kBarPA + h));
         }
         __syncwarp();
     } else if (warp < kMmaWarp) {
@@ -956,7 +972,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             }
             build_row(kcw, sK, 0u);
             fence_proxy_async();
-            mbar_arrive(bar(kBarK));
+            warp_arrive(bar(kBarK));
             const int vb = i & 1;
             if (i > 1) {   // the products of tile - 2 read this V_hat buffer
                 if (!warp_wait(bar(kBarVF0 + vb), (ph_vf >> vb) & 1u, fail)) break;
@@ -964,36 +980,42 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             }
             build_row(vcw, sV + (uint32_t)vb * kTileBytes, 128u);
             fence_proxy_async();
-            mbar_arrive(bar(kBarV0 + vb));
+            warp_arrive(bar(kBarV0 + vb));
             if (tile < t_last) load_codes((tile + 1) * kKeys, r);
         }
         __syncwarp();
     } else {
-        // ================= tensor-core issue (one lane)
-        if (lane == 0 && n_tiles > 0) {
+        // ================= tensor-core issue: the warp runs the loop (uniform
+        // waits and descriptors), one elected lane issues each instruction.
+        // A descriptor's start address is its low 14 bits (address / 16), so
+        // an operand offset is added to a base descriptor as offset / 16.
+        if (n_tiles > 0) {
+            const uint64_t dq0 = smem_desc(sQ), dq1 = smem_desc(sQ + kTileBytes);
+            const uint64_t dk = smem_desc(sK);
+            const uint64_t dv0 = smem_desc_mn(sV, kHalfTile), dv1 = smem_desc_mn(sV + kTileBytes, kHalfTile);
             auto issue_s = [&](int hh) {
-                const uint32_t sQh = sQ + (uint32_t)hh * kTileBytes;
+                const uint64_t dq = hh ? dq1 : dq0;
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
-                    mma_f16(tmem + (uint32_t)(hh * kKeys), smem_desc(sQh + off),
-                            smem_desc(sK + off), kIdesc, ks > 0);
+                    mma_ss_elect(tmem + (uint32_t)(hh * kKeys), dq + (off >> 4), dk + (off >> 4),
+                                 kIdesc, ks > 0);
                 }
-                mma_commit(bar(kBarSA + hh));
+                commit_elect(bar(kBarSA + hh));
             };
-            auto issue_pv = [&](int hh, uint32_t sVb, bool acc) {
+            auto issue_pv = [&](int hh, int vb, bool acc) {
+                const uint64_t dv = vb ? dv1 : dv0;
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
                     // A = P: keys 16 ks .. 16 ks + 15 in columns 8 ks .. 8 ks + 7
-                    mma_f16_ta(tmem + (uint32_t)(2 * kKeys + hh * kD),
-                               tmem + (uint32_t)(hh * kKeys + ks * 8),
-                               smem_desc_mn(sVb + (uint32_t)ks * 2048u, kHalfTile), kIdescBmn,
-                               (acc || ks > 0) ? 1u : 0u);
+                    mma_ts_elect(tmem + (uint32_t)(2 * kKeys + hh * kD),
+                                 tmem + (uint32_t)(hh * kKeys + ks * 8),
+                                 dv + (uint64_t)(ks * 128), kIdescBmn, (acc || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(kBarOA + hh));
+                commit_elect(bar(kBarOA + hh));
             };
             uint32_t ph_k = 0, ph_v = 0, ph_p[2] = {0u, 0u}, ph_o[2] = {0u, 0u};   // ph_v: bit b per buffer
-            bool ok = lone_wait(bar(kBarK), ph_k, fail);
+            bool ok = warp_wait(bar(kBarK), ph_k, fail);
             ph_k ^= 1;
             if (ok) {
                 tc_fence_after();
@@ -1002,29 +1024,28 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             }
             for (int tile = t_first; ok && tile <= t_last; ++tile) {
                 const int i = tile - t_first, vb = i & 1;
-                const uint32_t sVb = sV + (uint32_t)vb * kTileBytes;
                 const bool more = tile < t_last;
-                if (!(ok = lone_wait(bar(kBarV0 + vb), (ph_v >> vb) & 1u, fail))) break;
+                if (!(ok = warp_wait(bar(kBarV0 + vb), (ph_v >> vb) & 1u, fail))) break;
                 ph_v ^= 1u << vb;
-                if (!(ok = lone_wait(bar(kBarPA), ph_p[0], fail))) break;
+                if (!(ok = warp_wait(bar(kBarPA), ph_p[0], fail))) break;
                 ph_p[0] ^= 1;
                 tc_fence_after();
-                issue_pv(0, sVb, i > 0);
+                issue_pv(0, vb, i > 0);
                 if (more) {
-                    if (!(ok = lone_wait(bar(kBarK), ph_k, fail))) break;
+                    if (!(ok = warp_wait(bar(kBarK), ph_k, fail))) break;
                     ph_k ^= 1;
-                    if (!(ok = lone_wait(bar(kBarOA), ph_o[0], fail))) break;
+                    if (!(ok = warp_wait(bar(kBarOA), ph_o[0], fail))) break;
                     ph_o[0] ^= 1;
                     tc_fence_after();
                     issue_s(0);
                 }
-                if (!(ok = lone_wait(bar(kBarPB), ph_p[1], fail))) break;
+                if (!(ok = warp_wait(bar(kBarPB), ph_p[1], fail))) break;
                 ph_p[1] ^= 1;
                 tc_fence_after();
-                issue_pv(1, sVb, i > 0);
-                mma_commit(bar(kBarVF0 + vb));
+                issue_pv(1, vb, i > 0);
+                commit_elect(bar(kBarVF0 + vb));
                 if (more) {
-                    if (!(ok = lone_wait(bar(kBarOB), ph_o[1], fail))) break;
+                    if (!(ok = warp_wait(bar(kBarOB), ph_o[1], fail))) break;
                     ph_o[1] ^= 1;
                     tc_fence_after();
                     issue_s(1);
@@ -1032,11 +1053,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             }
             // every product issued completes before the output is read and
             // tensor memory is freed
-            mma_commit(bar(kBarDrain));
-            for (uint32_t it = 0; it < kWaitLimit; ++it) {
-                if (mbar_try(bar(kBarDrain), 0u)) break;
-                if (it + 1 == kWaitLimit) *fail = 1;
-            }
+            commit_elect(bar(kBarDrain));
+            bool drained = false;
+            for (uint32_t it = 0; it < kWaitLimit && !drained; ++it)
+                drained = __all_sync(0xffffffffu, mbar_try(bar(kBarDrain), 0u));
+            if (!drained && lane == 0) *fail = 1;
         }
         __syncwarp();
     }
