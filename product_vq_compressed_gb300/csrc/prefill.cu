@@ -571,17 +571,19 @@ size_t prefill_smem_bytes() {
 //     and is read from there as the A operand of O += P V_hat.
 //   * warps 8-11: rebuild of K~(j) (one buffer) and V_hat(j) (two buffers)
 //     from the codes, one key row per thread; codes of tile j+1 load ahead.
-//   * warp 12: tensor-memory allocation; one lane issues every tcgen05.mma
-//     in the order S_A(j), S_B(j), then per tile PV_A(j), S_A(j+1), PV_B(j),
-//     S_B(j+1).  A score block is overwritten only after the product that
-//     read its P has completed.
+//   * warp 12: tensor-memory allocation and every tcgen05.mma, in the order
+//     S_A(j), S_B(j), then per tile PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
+//     The whole warp runs the loop (its waits and operand descriptors stay
+//     warp-uniform) and one elected lane issues each instruction.  A score
+//     block is overwritten only after the product that read its P has
+//     completed.
 // Tensor memory (512 columns): S_A | S_B | O_A | O_B.  O stays in tensor
 // memory for the whole key range; when a row's reference maximum moves, the
 // softmax thread rescales its P columns already written in this tile and its
 // O row (the previous P V_hat of that head has completed by then: the score
 // block it waits for was issued after it).
 // Every wait is bounded and also gives up once another role has failed; the
-// verdict is CTA-wide (NaN rows), and the MMA lane drains its products
+// verdict is CTA-wide (NaN rows), and the MMA warp drains its products
 // before tensor memory is freed.
 
 constexpr int kPairThreads = 416;
@@ -591,9 +593,9 @@ constexpr int kPairCols = 512;    // tensor-memory columns
 enum PairBar {
     kBarSA, kBarSB,       // score block of head A / B complete (commit)
     kBarOA, kBarOB,       // P V_hat of head A / B complete (commit)
-    kBarPA, kBarPB,       // P of head A / B written (128 arrivals)
-    kBarK,                // K~ written (128 arrivals)
-    kBarV0, kBarV1,       // V_hat buffer 0 / 1 written (128 arrivals)
+    kBarPA, kBarPB,       // P of head A / B written (one arrival per warp)
+    kBarK,                // K~ written (one arrival per warp)
+    kBarV0, kBarV1,       // V_hat buffer 0 / 1 written (one arrival per warp)
     kBarVF0, kBarVF1,     // V_hat buffer 0 / 1 free again (commit)
     kBarDrain,            // every issued product complete (commit)
     kNumPairBars
