@@ -674,6 +674,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
+// 64 consecutive fp32 columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+          "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]),
+          "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]),
+          "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]),
+          "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -885,20 +911,29 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             const int j0 = tile * kKeys;
             const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
             float alpha_o = 1.f;   // rescale owed by this row's O
+            // the row in two 64-column halves (one tcgen05.ld each); P of half
+            // c goes to columns [32 c, 32 c + 32), all of them already read
 #pragma unroll 1
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float sv[32];
-                tmem_ld32(t_s + c * 32, sv);
+            for (int c = 0; c < kKeys / 64; ++c) {
+                float sv[64];
+                tmem_ld64(t_s + c * 64, sv);
                 if (!full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = j0 + c * 32 + i;
+                    for (int i = 0; i < 64; ++i) {
+                        const int j = j0 + c * 64 + i;
                         sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
                     }
                 }
-                float cmax = -INFINITY;
+                // four independent maximum chains
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) cmax = max3f(cmax, sv[i], sv[i + 1]);
+                for (int i = 0; i < 64; i += 8) {
+                    mx0 = max3f(mx0, sv[i], sv[i + 1]);
+                    mx1 = max3f(mx1, sv[i + 2], sv[i + 3]);
+                    mx2 = max3f(mx2, sv[i + 4], sv[i + 5]);
+                    mx3 = max3f(mx3, sv[i + 6], sv[i + 7]);
+                }
+                const float cmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 // the reference maximum moves only past kSlack (base 2)
                 const bool moves = cmax > m + kSlack;
                 if (__any_sync(0xffffffffu, moves)) {
@@ -910,7 +945,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                     }
                     // P columns already written in this tile, rescaled
                     if (c > 0) tmem_wait_st();
-                    for (int cc = 0; cc < c; ++cc) {
+                    for (int cc = 0; cc < 2 * c; ++cc) {
                         uint32_t pw[16];
                         tmem_ld16(t_s + cc * 16, pw);
 #pragma unroll
@@ -922,16 +957,24 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                     }
                 }
                 const float base_m = m == -INFINITY ? 0.f : m;
-                uint32_t pk[16];
-                float ls = 0.f;
+                float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = ex2(sv[i] - base_m), p1 = ex2(sv[i + 1] - base_m);
-                    ls += p0 + p1;
-                    pk[i / 2] = pack_h2(p0, p1);
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float p0 = ex2(sv[q * 32 + i] - base_m);
+                        const float p1 = ex2(sv[q * 32 + i + 1] - base_m);
+                        const float p2 = ex2(sv[q * 32 + i + 2] - base_m);
+                        const float p3 = ex2(sv[q * 32 + i + 3] - base_m);
+                        ls0 += p0 + p1;
+                        ls1 += p2 + p3;
+                        pk[i / 2] = pack_h2(p0, p1);
+                        pk[i / 2 + 1] = pack_h2(p2, p3);
+                    }
+                    tmem_st16(t_s + c * 32 + q * 16, pk);
                 }
-                l += ls;
-                tmem_st16(t_s + c * 16, pk);
+                l += ls0 + ls1;
             }
             // the row's O (all earlier tiles' P V_hat, complete) follows the
             // moved maximum; on the first tile the product overwrites O
