@@ -73,3 +73,26 @@ def test_prefill_growing_scores_move_the_maximum(H_q, H_kv, causal):
     ok, err, _ = parity.allclose_report(out.cpu().numpy().astype(np.float64),
                                         oracle.to_f16(ref).astype(np.float64))
     assert ok, f"max |err| {err}"
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(4, 2), (3, 3)])
+def test_prefill_empty_cache_batch_is_zero(H_q, H_kv):
+    """A batch holding no keys (kv_lens 0): its CTAs have no key tile and
+    write exact zeros; the other batch is the oracle's attention over its
+    own length."""
+    D, N, S_kv, S_q = 128, 256, 400, 130
+    spec = small_spec(31 + H_q, B=2, H_q=H_q, H_kv=H_kv, D=D, S_kv=S_kv, S_q=S_q,
+                      causal=True, draw_keys=False, draw_values=False, draw_codes=True)
+    inp = make_inputs(spec)
+    lens = torch.tensor([0, 333], dtype=torch.int32, device="cuda:0")
+    out = vq.prefill_attend(dev(inp["q"]), dev(inp["k_codes"]), dev(inp["k_codebook"]),
+                            dev(inp["v_codes"]), dev(inp["v_codebook"]), dev(inp["smooth"]),
+                            spec.sm_scale, causal=True, kv_lens=lens)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(got[0] == 0.0)
+    ref = oracle.attend(inp["q"][1:], inp["k_codes"][1:, :, :333], inp["k_codebook"],
+                        inp["v_codes"][1:, :, :333], inp["v_codebook"], inp["smooth"],
+                        spec.sm_scale, True, 0)
+    ok, err, _ = parity.allclose_report(got[1:], oracle.to_f16(ref).astype(np.float64))
+    assert ok, f"max |err| {err}"
