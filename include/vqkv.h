@@ -246,8 +246,11 @@ VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
  * Same operation through the tcgen05 tensor-core path (key/value tiles
  * rebuilt from codes in shared memory, Q~K~^T and PV on the tensor cores,
  * accumulators in tensor memory).  Used when S_q >= 64; smaller S_q, or
- * shapes outside the tensor-core kernel's limits (D != 128, sub_dim != 4),
- * are served by vq_decode_attend with the same arguments.  Page: "Metal
+ * shapes outside the tensor-core kernel's limits (D != 128, sub_dim != 4,
+ * codes wider than one byte), are served by vq_decode_attend with the same
+ * arguments.  An even GQA group size H_q / H_kv runs two query heads of a
+ * KV group per block (sharing the rebuilt tiles); an odd one runs one head
+ * per block.  Page: "Metal
  * Kernels API", section "Fused SDPA", metal_fused_sdpa; the prefill-shaped
  * tile loop follows the companion described under rabitq_prefill_attend.
  * Errors as vq_decode_attend.
