@@ -8,33 +8,20 @@
 // the companion kernel described under rabitq_prefill_attend (both products
 // on matrix tiles, keys and values decoded inside the tile loop).
 //
-// One CTA = (batch, query head, tile of 128 query rows), 256 threads: query
-// row i (tensor-memory lane i of every accumulator) belongs to threads i and
-// i + 128, which take the two 64-column halves of its scores and output.
+// The kernel below (prefill_pair_kernel) serves every GQA group size:
 //   * Q~ = Hn (q (.) s_g^-1) * scale * log2(e) is built once per CTA (FWHT in
 //     registers) and stored as the A operand in the canonical K-major,
 //     128-byte-swizzled shared-memory layout (fp16).
-//   * For every tile of 128 keys the CTA rebuilds, from the uint8 codes and
-//     fp16 codebook replicas in shared memory, K~ and V_hat as [keys x D]
-//     tiles (one key row per thread, 128-byte swizzle): K~ is the K-major B
-//     operand of S = Q~ K~^T, V_hat the MN-major B operand of O = P V_hat.
-//   * One thread issues tcgen05.mma (kind::f16, M = N = 128, K = 16 per
-//     instruction, fp32 accumulate) into tensor memory and commits to an
-//     mbarrier; every thread reads its row back with tcgen05.ld.
-//   * Online softmax in base 2 per row over the score row in tensor memory
-//     (see below); P (fp16) goes to shared memory as the A
-//     operand of the second product; the running output stays in registers
-//     (O = O * alpha + P V_hat per tile).
+//   * For every tile of 128 keys, K~ and V_hat are rebuilt from the uint8
+//     codes and fp16 codebook replicas in shared memory as [keys x D] tiles
+//     (one key row per thread, 128-byte swizzle): K~ is the K-major B operand
+//     of S = Q~ K~^T, V_hat the MN-major B operand of O = P V_hat.
+//   * tcgen05.mma kind::f16, M = N = 128, K = 16 per instruction, fp32
+//     accumulation in tensor memory.
+//   * Online softmax in base 2 per row, with a reference maximum that moves
+//     only when a score exceeds it by more than 2^8.
 //   * Key tiles that no row of the CTA can see are skipped; masks are applied
 //     only on tiles that need them.
-//   * Pipelining: while the tensor cores compute Q~K~^T of tile j, the
-//     threads rebuild V_hat of tile j and load the codes of tile j+1; while
-//     they compute P V_hat of tile j, the threads rebuild K~ of tile j+1.  One
-//     thread polls each mbarrier; the others wait at the block barrier that
-//     follows.
-//   * Softmax keeps a reference maximum per row that moves only when a score
-//     exceeds it by more than 2^8: one pass over the scores in tensor memory,
-//     a second only when the maximum moves.
 // Every mbarrier wait is bounded: if one expires the CTA writes NaN rows,
 // waits (bounded) for its own MMAs once more, frees its tensor memory and
 // exits, so a fault shows up in the output instead of hanging the GPU.
@@ -48,7 +35,6 @@ namespace {
 constexpr int kRows = 128;        // query rows per CTA (MMA M)
 constexpr int kKeys = 128;        // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;           // head dimension of this kernel
-constexpr int kThreads = 256;     // two threads per query row (column halves)
 constexpr int kSub = 4;           // sub-vector size of both codebooks
 constexpr uint32_t kTileBytes = kRows * kD * 2;  // one fp16 operand tile, 32 KiB
 constexpr uint32_t kHalfTile = kTileBytes / 2;   // 64-element K half, 16 KiB
@@ -64,20 +50,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-
-// Bounded wait for phase `parity` of the mbarrier; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-        if (done) return true;
-    }
-    return false;
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -119,20 +91,6 @@ __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t mn_str
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kKeys >> 3) << 17) |
                             ((uint32_t)(kRows >> 4) << 24);
 constexpr uint32_t kIdescBmn = kIdesc | (1u << 16);
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
-        ::"r"(bar) : "memory");
-}
 
 // 32 consecutive fp32 columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
@@ -205,366 +163,14 @@ struct PrefillArgs {
     __half *out;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    // 1024-byte aligned operand tiles: Q~ | K~ | V_hat | P | tables | misc
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    unsigned char *gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base, sK = base + kTileBytes, sV = base + 2 * kTileBytes,
-                   sP = base + 3 * kTileBytes, sTab = base + 4 * kTileBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 4 * kTileBytes + kTabBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
-    float *red = reinterpret_cast<float *>(bars + 4);   // [2][kRows] row exchange
-    int *flg = reinterpret_cast<int *>(red + 2 * kRows); // [2][kRows] "maximum moves"
-    const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
-
-    // thread = (row r of the tile, column half hh); warps w and w + 4 share
-    // the tensor-memory lanes of rows 32 (w mod 4) ..
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int r = tid & (kRows - 1), hh = tid >> 7;
-    const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
-    const int g = hq / a.G;
-    const int q0 = qt * kRows;
-    const int row = q0 + r;                // this thread's query row
-    const bool row_ok = row < a.S_q;
-
-    // ---- tensor memory: S in columns [0, 128), P V_hat in [128, 256)
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
-                     ::"r"(smem_u32(tmem_slot)), "r"(256));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-    }
-    if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-
-    // ---- fp16 codebook replicas: row c = key centroid c x16 | value centroid c x16.
-    //      A thread owns a row: both centroid loads in flight, then 16 stores.
-    //      The barrier publishes the table to the rebuilds of every thread.
-    for (int c = tid; c < 256; c += kThreads) {
-        uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
-        if (c < a.Nk) {
-            const float4 f = *reinterpret_cast<const float4 *>(a.kcb + c * kSub);
-            k0 = pack_h2(f.x, f.y);
-            k1 = pack_h2(f.z, f.w);
-        }
-        if (c < a.Nv) {
-            const float4 f = *reinterpret_cast<const float4 *>(a.vcb + c * kSub);
-            v0 = pack_h2(f.x, f.y);
-            v1 = pack_h2(f.z, f.w);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
-            sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
-        }
-    }
-    __syncthreads();
-
-    // ---- Q~ row r (fp16, swizzled A operand).  Thread (r, hh) transforms
-    //      dims [64 hh, 64 hh + 64) of row r: smooth reciprocals from shared
-    //      memory, butterflies h = 1 .. 32 in registers, then stage h = 64
-    //      pairs the two halves through a transposed exchange in the V_hat /
-    //      P region (unused until the loop): x[i], x[i + 64] -> sum, difference.
-    float *rs = reinterpret_cast<float *>(flg + 2 * kRows);   // [kD] 1 / s_g
-    float *xch = reinterpret_cast<float *>(gbase + 2 * kTileBytes);   // [kD][kRows]
-    if (tid < kD) {
-        const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
-        rs[tid] = a.smooth_mode != 0 ? 1.f / sp[tid] : 1.f;
-    }
-    __syncthreads();
-    {
-        constexpr int kH = kD / 2;
-        float x[kH];
-        if (row_ok) {
-            const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD + hh * kH;
-#pragma unroll
-            for (int e = 0; e < kH; e += 8) {
-                const uint4 raw4 = *reinterpret_cast<const uint4 *>(qp + e);
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw4);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __half22float2(h2[k]);
-                    x[e + 2 * k] = f.x * rs[hh * kH + e + 2 * k];
-                    x[e + 2 * k + 1] = f.y * rs[hh * kH + e + 2 * k + 1];
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < kH; ++e) x[e] = 0.f;
-        }
-#pragma unroll
-        for (int h = 1; h < kH; h <<= 1) {
-#pragma unroll
-            for (int i = 0; i < kH; ++i) {
-                if ((i & h) == 0) {
-                    const float u = x[i], v = x[i + h];
-                    x[i] = u + v;
-                    x[i + h] = u - v;
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < kH; ++e) xch[(hh * kH + e) * kRows + r] = x[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < kH; ++e) {
-            const float other = xch[((1 - hh) * kH + e) * kRows + r];
-            x[e] = hh == 0 ? x[e] + other : other - x[e];
-        }
-#pragma unroll
-        for (int ch = 0; ch < kH / 8; ++ch) {
-            const float *p = x + ch * 8;
-            sts128(sQ + sw_off(r, hh * (kH / 8) + ch), pack_h2(p[0] * a.qscale, p[1] * a.qscale),
-                   pack_h2(p[2] * a.qscale, p[3] * a.qscale),
-                   pack_h2(p[4] * a.qscale, p[5] * a.qscale),
-                   pack_h2(p[6] * a.qscale, p[7] * a.qscale));
-        }
-    }
-
-    // ---- visible keys of this row and of the CTA (batch b holds L keys)
-    const int L = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
-    const int q_abs = L - a.S_q + row;
-    int hi = a.causal ? q_abs : L - 1;
-    hi = min(hi, L - 1);
-    int lo = a.window > 0 ? max(0, q_abs - a.window + 1) : 0;
-    if (!row_ok) { lo = 1; hi = 0; }
-    const int last_row = min(q0 + kRows, a.S_q) - 1;
-    const int qa_first = L - a.S_q + q0, qa_last = L - a.S_q + last_row;
-    const int cta_lo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
-    const int cta_hi = min(a.causal ? qa_last : L - 1, L - 1);
-    const int all_lo = a.window > 0 ? max(0, qa_last - a.window + 1) : 0;   // seen by every row
-    const int all_hi = min(a.causal ? qa_first : L - 1, L - 1);
-    const int t_first = cta_lo / kKeys;
-    const int t_last = cta_hi < cta_lo ? t_first - 1 : cta_hi / kKeys;   // none: empty range
-
-    constexpr int kHalfD = kD / 2, kHalfKeys = kKeys / 2;
-    float o[kHalfD];                       // output dims hh*64 .. hh*64+63
-#pragma unroll
-    for (int e = 0; e < kHalfD; ++e) o[e] = 0.f;
-    float m = -INFINITY, l = 0.f;          // l: this half's share of the row sum
-    uint32_t ph_s = 0, ph_o = 0;
-    bool failed = false;
-
-    const int64_t bg = (int64_t)b * a.H_kv + g;
-    const uint8_t *kcodes = a.kc + bg * a.stride * 32 + hh * 16;
-    const uint8_t *vcodes = a.vc + bg * a.stride * 32 + hh * 16;
-
-    // codes of one tile in registers: the 16 codes (dims hh*64 ..) of the
-    // tile's key r, K and V side
-    uint32_t kcw[4], vcw[4];
-    auto load_codes = [&](int j0) {
-        const int j = min(j0 + r, a.S_kv - 1);
-        const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
-        const uint4 d0 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32);
-        kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
-        vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
-    };
-    // Half hh of row r (the tile's key r) of a [keys x D] fp16 tile: 16
-    // centroids, two per 16-byte chunk, 128-byte swizzle.  The same image
-    // serves as K~ (B of Q~K~^T, K-major) and as V_hat (B of P V_hat, read
-    // MN-major: keys along K, dims contiguous).
-    auto build_rows = [&](const uint32_t *cw, uint32_t dst, uint32_t half_off) {
-        const uint32_t lane_off = half_off + (uint32_t)((tid & 15) * 8);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            const uint32_t w = cw[cc >> 1];
-            const int i0 = (cc & 1) * 2;
-            const uint2 e0 = lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)i0 << 4)));
-            const uint2 e1 =
-                lds64(sTab + __byte_perm(w, lane_off, 0x6504u | ((uint32_t)(i0 + 1) << 4)));
-            sts128(dst + sw_off(r, hh * 8 + cc), e0.x, e0.y, e1.x, e1.y);
-        }
-    };
-    auto build_k = [&]() { build_rows(kcw, sK, 0u); };
-    auto build_v = [&](uint32_t sVb) { build_rows(vcw, sVb, 128u); };
-
-    // ---- first tile's K~, then the pipelined loop:
-    //   QK(j) on the tensor cores   || V_hat(j) rebuilt, codes of tile j+1 loading
-    //   softmax(j) -> P
-    //   PV(j) on the tensor cores   || K~(j+1) rebuilt
-    //   O = O * alpha + PV(j)
-    // Each rebuild half runs under one product, and V_hat needs one buffer:
-    // PV(j-1) has completed before V_hat(j) is written.
-    if (t_first <= t_last) {
-        load_codes(t_first * kKeys);
-        build_k();
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lanes + (uint32_t)(hh * kHalfKeys);
-    const uint32_t t_o = tmem + lanes + (uint32_t)(kKeys + hh * kHalfD);
-
-    for (int tile = t_first; tile <= t_last; ++tile) {
-        const int j0 = tile * kKeys;
-        const uint32_t sVj = sV;
-        // ---- S = Q~ K~^T into tensor memory
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
-                mma_f16(tmem, smem_desc(sQ + off), smem_desc(sK + off), kIdesc, ks > 0);
-            }
-            mma_commit(bar_s);
-        }
-        build_v(sVj);                 // from this tile's value codes
-        if (tile < t_last) load_codes(j0 + kKeys);
-        // one thread polls (bounded); the block-wide verdict keeps every
-        // thread on the same path
-        bool ok = true;
-        if (tid == 0) ok = mbar_wait(bar_s, ph_s);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_s ^= 1;
-        tc_fence_after();
-
-        // ---- online softmax of row r over this tile, each half 64 keys.
-        //      The row's reference maximum m moves only when a score exceeds
-        //      it by more than kSlack (base 2).  One pass computes P against
-        //      the current m; if the row's m must move (always on its first
-        //      visible tile), the halves agree on the new maximum through
-        //      shared memory and P is recomputed.  Otherwise P = 2^(s - m) <=
-        //      2^kSlack, which fp16 holds at full relative precision.
-        const bool full = j0 >= all_lo && j0 + kKeys - 1 <= all_hi;
-        const int jh = j0 + hh * kHalfKeys;
-        auto p_pass = [&](float base, float &mxv) {
-            float ls = 0.f;
-#pragma unroll
-            for (int c = 0; c < kHalfKeys / 32; ++c) {
-                float sv[32];
-                tmem_ld32(t_s + c * 32, sv);
-                if (!full) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = jh + c * 32 + i;
-                        sv[i] = (j >= lo && j <= hi) ? sv[i] : -INFINITY;
-                    }
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    mxv = max3f(mxv, sv[i], sv[i + 1]);
-                    const float p0 = ex2(sv[i] - base), p1 = ex2(sv[i + 1] - base);
-                    ls += p0 + p1;
-                    pk[i / 2] = pack_h2(p0, p1);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    sts128(sP + sw_off(r, hh * 8 + c * 4 + q), pk[4 * q], pk[4 * q + 1],
-                           pk[4 * q + 2], pk[4 * q + 3]);
-            }
-            return ls;
-        };
-        float mx = -INFINITY;
-        float lsum = p_pass(m == -INFINITY ? 0.f : m, mx);
-        const bool half_moves = mx > m + kSlack;
-        red[hh * kRows + r] = mx;
-        flg[hh * kRows + r] = half_moves ? 1 : 0;
-        // one barrier publishes P (common case) and tells whether any row of
-        // the CTA must move its maximum
-        fence_proxy_async();
-        tc_fence_before();
-        float alpha = 1.f;
-        if (__syncthreads_or(half_moves)) {
-            const bool row_moves = (flg[r] | flg[kRows + r]) != 0;
-            if (__any_sync(0xffffffffu, row_moves)) {   // tcgen05.ld is warp-collective
-                const float m_new = row_moves ? fmaxf(m, fmaxf(red[r], red[kRows + r])) : m;
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                if (row_moves) alpha = ex2(m - m_use);
-                m = m_new;
-                float unused = -INFINITY;
-                lsum = p_pass(m_use, unused);
-            }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-        }
-        l = l * alpha + lsum;
-        // ---- P V_hat into tensor memory, next tile's operands meanwhile
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-                // A = P (K-major, keys along K); B = V_hat rows (keys) of 16
-                // keys = two 8-row groups per step, MN-major
-                const uint32_t off = (uint32_t)((ks >> 2) * kHalfTile + (ks & 3) * 32);
-                mma_f16(tmem + kKeys, smem_desc(sP + off),
-                        smem_desc_mn(sVj + (uint32_t)ks * 2048u, kHalfTile), kIdescBmn, ks > 0);
-            }
-            mma_commit(bar_o);
-        }
-        if (tile < t_last) {
-            build_k();
-            fence_proxy_async();
-        }
-        ok = true;
-        if (tid == 0) ok = mbar_wait(bar_o, ph_o);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_o ^= 1;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < kHalfD / 32; ++c) {
-            float pv[32];
-            tmem_ld32(t_o + c * 32, pv);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, pv[i]);
-        }
-        tc_fence_before();
-    }
-
-    // ---- output row: the two halves' sums combine into the row's l
-    __syncthreads();
-    red[hh * kRows + r] = l;
-    __syncthreads();
-    l = red[r] + red[kRows + r];
-    if (row_ok) {
-        __half *op = a.out + (((int64_t)b * a.H_q + hq) * a.S_q + row) * kD + hh * kHalfD;
-        const float inv = failed ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
-#pragma unroll
-        for (int ch = 0; ch < kHalfD / 8; ++ch) {
-            const float *p = o + ch * 8;
-            uint4 v;
-            v.x = pack_h2(p[0] * inv, p[1] * inv);
-            v.y = pack_h2(p[2] * inv, p[3] * inv);
-            v.z = pack_h2(p[4] * inv, p[5] * inv);
-            v.w = pack_h2(p[6] * inv, p[7] * inv);
-            *reinterpret_cast<uint4 *>(op + ch * 8) = v;
-        }
-    }
-    if (failed && tid == 0) {   // let MMAs still in flight finish before freeing
-        mbar_wait(bar_s, ph_s);
-        mbar_wait(bar_o, ph_o);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n"
-                     ::"r"(tmem), "r"(256));
-    }
-}
-
-size_t prefill_smem_bytes() {
-    return 4 * (size_t)kTileBytes + kTabBytes + 32 + 2 * kRows * (sizeof(float) + sizeof(int)) +
-           kD * sizeof(float) +
-           1024;   // + alignment slack
-}
-
-
 // ------------------------------------------------------------------ two heads per CTA
 //
 // prefill_pair_kernel: one CTA = (batch, two query heads of one KV group,
-// tile of 128 query rows), 416 threads in four roles.  The two heads share
-// the rebuilt K~ and V_hat tiles of their KV head, and the two heads'
-// products and softmaxes interleave so that the tensor cores run one head's
-// product while the CUDA cores run the other head's softmax.
+// tile of 128 query rows), 416 threads in four roles; an odd group's last
+// pair has a single head (head B's warps idle, its products skipped).  The
+// two heads share the rebuilt K~ and V_hat tiles of their KV head, and the
+// two heads' products and softmaxes interleave so that the tensor cores run
+// one head's product while the CUDA cores run the other head's softmax.
 //   * warps 0-3 / 4-7: softmax of head A / head B; thread = query row r
 //     (tensor-memory lane r), the whole 128-score row of a tile.  P (fp16) is
 //     written back into the first 64 columns of the row's own score columns
@@ -758,8 +364,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qt = blockIdx.x, b = blockIdx.z;
-    const int hq0 = 2 * blockIdx.y;   // heads hq0 (A) and hq0 + 1 (B): one KV group
-    const int g = hq0 / a.G;
+    // blockIdx.y = (KV group g, pair of its query heads): heads hq0 (A) and
+    // hq0 + 1 (B); an odd group's last pair has no head B
+    const int pairs = (a.G + 1) / 2;
+    const int g = blockIdx.y / pairs;
+    const int hq0 = g * a.G + 2 * (blockIdx.y - g * pairs);
+    const bool has_b = hq0 + 1 < (g + 1) * a.G;
     const int q0 = qt * kRows;
 
     if (warp == kMmaWarp) {
@@ -835,7 +445,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
         vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
     };
 
-    if (warp < kRebuildWarp) {
+    if (warp < kRebuildWarp && (warp < 4 || has_b)) {
         // ---- Q~ row r of head h (fp16, swizzled A operand): each half's
         //      butterflies below 64 in registers, the first half parked in
         //      the K~ / V_hat region (free until the loop), then the stage
@@ -898,13 +508,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
     if (warp < kRebuildWarp) {
         // ================= softmax of head h, row r
         const int q_abs = L - a.S_q + row;
+        const int t_end = h == 0 || has_b ? t_last : t_first - 1;   // no head B: no tiles
         int hi = a.causal ? q_abs : L - 1;
         hi = min(hi, L - 1);
         int lo = a.window > 0 ? max(0, q_abs - a.window + 1) : 0;
         if (row >= a.S_q) { lo = 1; hi = 0; }
         float m = -INFINITY;
         uint32_t ph = 0;
-        for (int tile = t_first; tile <= t_last; ++tile) {
+        for (int tile = t_first; tile <= t_end; ++tile) {
             if (!warp_wait(bar(kBarSA + h), ph, fail)) break;
             ph ^= 1;
             tc_fence_after();
@@ -1011,8 +622,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
         uint32_t ph_sb = 0, ph_vf = 0;   // ph_vf: bit b = parity of V_hat buffer b
         for (int tile = t_first; tile <= t_last; ++tile) {
             const int i = tile - t_first;
-            if (i > 0) {   // both score blocks of the previous tile read K~
-                if (!warp_wait(bar(kBarSB), ph_sb, fail)) break;
+            if (i > 0) {   // the score blocks of the previous tile read K~
+                if (!warp_wait(bar(has_b ? kBarSB : kBarSA), ph_sb, fail)) break;
                 ph_sb ^= 1;
             }
             build_row(kcw, sK, 0u);
@@ -1065,7 +676,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
-                issue_s(1);
+                if (has_b) issue_s(1);
             }
             for (int tile = t_first; ok && tile <= t_last; ++tile) {
                 const int i = tile - t_first, vb = i & 1;
@@ -1084,12 +695,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                     tc_fence_after();
                     issue_s(0);
                 }
-                if (!(ok = warp_wait(bar(kBarPB), ph_p[1], fail))) break;
-                ph_p[1] ^= 1;
-                tc_fence_after();
-                issue_pv(1, vb, i > 0);
+                if (has_b) {
+                    if (!(ok = warp_wait(bar(kBarPB), ph_p[1], fail))) break;
+                    ph_p[1] ^= 1;
+                    tc_fence_after();
+                    issue_pv(1, vb, i > 0);
+                }
                 commit_elect(bar(kBarVF0 + vb));
-                if (more) {
+                if (more && has_b) {
                     if (!(ok = warp_wait(bar(kBarOB), ph_o[1], fail))) break;
                     ph_o[1] ^= 1;
                     tc_fence_after();
@@ -1110,7 +723,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
     __syncthreads();   // every role has left its loop; every product has completed
     tc_fence_after();
 
-    if (warp < kRebuildWarp) {
+    if (warp < kRebuildWarp && (h == 0 || has_b)) {
         // ---- output row r of head h (tcgen05.ld is warp-collective: every
         //      lane loads, only rows of the query block are stored)
         const bool failed = *fail != 0;
@@ -1184,23 +797,13 @@ cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream) {
     p.kv_lens = a.kv_lens;
     p.out = reinterpret_cast<__half *>(a.out_f16);
     const unsigned q_tiles = (unsigned)((a.S_q + kRows - 1) / kRows);
-    if (p.G % 2 == 0) {   // two query heads of one KV group per CTA
-        const size_t smem = prefill_pair_smem_bytes();
-        cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
-        if (err != cudaSuccess) return err;
-        dim3 grid(q_tiles, (unsigned)(a.H_q / 2), (unsigned)a.B);
-        prefill_pair_kernel<<<grid, kPairThreads, smem, stream>>>(p);
-        return cudaGetLastError();
-    }
-    const size_t smem = prefill_smem_bytes();
-    cudaError_t err = cudaFuncSetAttribute(prefill_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    // up to two query heads of one KV group per CTA
+    const size_t smem = prefill_pair_smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(q_tiles, (unsigned)a.H_q, (unsigned)a.B);
-    prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
+    dim3 grid(q_tiles, (unsigned)(a.H_kv * ((p.G + 1) / 2)), (unsigned)a.B);
+    prefill_pair_kernel<<<grid, kPairThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

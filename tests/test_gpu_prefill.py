@@ -1,8 +1,8 @@
 """GPU parity of the tensor-core prefill kernels against the float64 oracle.
 
 Query blocks of 64 rows or more with D = 128, 4-dimensional sub-vectors and
-uint8 codes take the tensor-core path: two query heads of a KV group per CTA
-when the group size is even, one head per CTA otherwise.  The cases span
+uint8 codes take the tensor-core path: two query heads of a KV group per CTA,
+and a single head in the last CTA of an odd group.  The cases span
 several key tiles with ragged tails, windows and causal bounds that cut
 tiles, the three smooth modes, and a cache whose scores grow along the keys
 so that every row's reference maximum moves between and within key tiles
@@ -27,8 +27,8 @@ CASES = [
     (1, 8, 1, 517, 64, False, 0, 1),       # group 8, not causal
     (1, 4, 2, 128, 128, True, 0, 0),       # one key tile exactly
     (1, 2, 1, 4101, 96, True, 1000, 2),    # long cache, window
-    (1, 4, 4, 333, 130, True, 0, 0),       # group 1: one head per CTA
-    (1, 6, 2, 450, 256, True, 129, 2),     # group 3: one head per CTA
+    (1, 4, 4, 333, 130, True, 0, 0),       # group 1: single-head CTAs
+    (1, 6, 2, 450, 256, True, 129, 2),     # group 3: a pair and a single head
 ]
 
 
@@ -79,7 +79,7 @@ def test_prefill_growing_scores_move_the_maximum(H_q, H_kv, causal):
 def test_prefill_empty_cache_batch_is_zero(H_q, H_kv):
     """A batch holding no keys (kv_lens 0): its CTAs have no key tile and
     write exact zeros; the other batch is the oracle's attention over its
-    own length."""
+    own length (even and odd group sizes)."""
     D, N, S_kv, S_q = 128, 256, 400, 130
     spec = small_spec(31 + H_q, B=2, H_q=H_q, H_kv=H_kv, D=D, S_kv=S_kv, S_q=S_q,
                       causal=True, draw_keys=False, draw_values=False, draw_codes=True)
