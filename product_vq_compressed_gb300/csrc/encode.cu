@@ -26,7 +26,11 @@
 //      the two are closer than twice a rigorous bound on the fp32 error of
 //      that form, the sub-vector is rescanned with the direct form
 //      sum_t (y_t - c_t)^2, so every decision is the one the direct form
-//      makes.  Codes are written in sub-vector order (coalesced stores);
+//      makes.  The decision is then certified against the rounding of the
+//      fp32 rotation and distances (code_certified); the few sub-vectors
+//      that are not certified are decided again in float-float arithmetic
+//      by the whole warp (nearest_exact).  Codes are written in sub-vector order (coalesced
+//      stores);
 //   3. optional reconstruction: the chosen centroids replace the sub-vectors
 //      in shared memory, one warp per token runs the FWHT again (Hn is
 //      symmetric and its own inverse), divides by the smooth factors and
@@ -92,6 +96,9 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
     // packed codes (CodeT = uint32_t): the tile's token rows, assembled here
     constexpr bool kPacked = std::is_same<CodeT, uint32_t>::value;
     uint32_t *ptile = reinterpret_cast<uint32_t *>(y_s + kSlots * SUBD);
+    // rotation error bound of every token of the tile (<= 256 tokens)
+    float *delta_s = reinterpret_cast<float *>(ptile + 768);
+    const float dcoef = rotation_delta_coef(p.log2D, inv_sqrt_d);
 
     if (tid == 0) *maxn2_s = 0.f;
     for (int i = tid; i < N * SUBD; i += kEncThreads) cb_s[i] = -2.0f * p.codebook[i];
@@ -125,6 +132,7 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                 const int h = token_head(p, v);
                 const float *sm = p.smooth_mode == 2 ? p.smooth + (size_t)h * D
                                                      : p.smooth;
+                float asum = 0.f;   // sum |fl(x s)|: size of the rotation's rounding error
                 for (int e = lane * 4; e < D; e += 128) {
                     const uint2 raw = *reinterpret_cast<const uint2 *>(xv + e);
                     const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
@@ -135,15 +143,20 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                             const float4 s = *reinterpret_cast<const float4 *>(sm + e);
                             f.x *= s.x; f.y *= s.y; f.z *= s.z; f.w *= s.w;
                         }
+                        asum += fabsf(f.x) + fabsf(f.y) + fabsf(f.z) + fabsf(f.w);
                         f.x *= inv_sqrt_d; f.y *= inv_sqrt_d;
                         f.z *= inv_sqrt_d; f.w *= inv_sqrt_d;
                     }
                     *reinterpret_cast<float4 *>(yv + e) = f;
                 }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, off);
+                if (lane == 0) delta_s[t] = asum * dcoef;
                 __syncwarp();
                 if (p.rotate) warp_fwht(yv, D, lane);
             } else {
                 for (int e = lane; e < D; e += 32) yv[e] = 0.f;
+                if (lane == 0) delta_s[t] = 0.f;
             }
         }
         if constexpr (kPacked) {
@@ -228,18 +241,36 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                 }
             }
             // When the two best screened values are closer than twice the
-            // fp32 error bound of the expanded form, order them exactly:
-            // rescan with the direct form sum_t (y_t - c_t)^2 (c = -cb/2).
+            // fp32 error bound of the expanded form, or the screen cannot
+            // certify the decision, rescan with the direct form
+            // sum_t (y_t - c_t)^2 (c = -cb/2).
+            // The decision is then certified (code_certified) from a lower
+            // bound on the other candidates' distances and an upper bound on
+            // the winner's, both to the fp32 sub-vector y~.
             const float maxn2 = *maxn2_s;
+            const int64_t lim = p.n_vec * n_sub;
+            bool cert[kR];
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
+                const int sl = tid + r * kEncThreads;
+                const float delta = delta_s[sl >> lsub];
                 float ny2 = 0.f;
 #pragma unroll
                 for (int t = 0; t < SUBD; ++t) ny2 = fmaf(y[r][t], y[r][t], ny2);
                 const float bound = (4.0f * SUBD + 8.0f) * 5.9604645e-8f *
                                     (maxn2 + 2.0f * sqrtf(maxn2 * ny2) + 1e-30f);
-                if (f2[r] - f1[r] <= 2.0f * bound) {
-                    float best = INFINITY;
+                // screened values are within `bound` of the exact f_c; |y~|^2
+                // within (SUBD + 8) u of ny2 with the sums' rounding
+                const float slack = (float)(SUBD + 8) * 5.9604645e-8f;
+                const float hi = (f1[r] + ny2) + (bound + slack * (fabsf(f1[r]) + ny2));
+                const float lo = f2[r] < INFINITY
+                                     ? (f2[r] + ny2) - (bound + slack * (fabsf(f2[r]) + ny2))
+                                     : INFINITY;
+                cert[r] = f2[r] - f1[r] > 2.0f * bound && code_certified<SUBD>(hi, lo, delta);
+                if (!cert[r]) {
+                    // rescan in the direct form: the order of the direct form,
+                    // and every candidate's distance for the certificate
+                    float best = INFINITY, second = INFINITY;
                     int bi = 0;
                     for (int c = 0; c < N; ++c) {
                         float d = 0.f;
@@ -248,12 +279,30 @@ encode_kernel(EncodeParams p, float inv_sqrt_d) {
                             const float e = y[r][t] + 0.5f * cb_s[c * SUBD + t];
                             d = fmaf(e, e, d);
                         }
+                        second = fminf(second, fmaxf(best, d));
                         if (d < best) { best = d; bi = c; }
                     }
                     i1[r] = bi;
+                    cert[r] = code_certified<SUBD>(best, second, delta);
+                }
+                cert[r] = cert[r] || v0 * n_sub + sl >= lim;
+            }
+            // sub-vectors the fp32 arithmetic cannot certify: float-float, whole warp
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                unsigned m = __ballot_sync(0xffffffffu, !cert[r]);
+                while (m) {
+                    const int src = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int sl = warp * 32 + src + r * kEncThreads;
+                    // cb_s holds -2 c (exact), so -0.5 cb_s is the centroid
+                    const int cx = nearest_exact_token<SUBD>(
+                        p, v0 + (sl >> lsub), sl & (n_sub - 1),
+                        [cb_s](int c, int t) { return -0.5f * cb_s[c * SUBD + t]; },
+                        delta_s[sl >> lsub], lane);
+                    if (lane == src) i1[r] = cx;
                 }
             }
-            const int64_t lim = p.n_vec * n_sub;
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 const int sl = tid + r * kEncThreads;
@@ -383,7 +432,8 @@ size_t encode_smem_bytes(int N, int sub_dim) {
     return sizeof(float) * ((((size_t)N * sub_dim + 3) & ~(size_t)3) +
                             (((size_t)N + 3) & ~(size_t)3) + 4 +
                             (size_t)kSlots * sub_dim) +
-           sizeof(uint32_t) * 768;   // packed token rows of a tile (<= 512 / n_sub x words)
+           sizeof(uint32_t) * 768 +  // packed token rows of a tile (<= 512 / n_sub x words)
+           sizeof(float) * 256;      // rotation error bound per token (<= 512 / n_sub tokens)
 }
 
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream) {

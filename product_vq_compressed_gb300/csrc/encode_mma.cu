@@ -32,8 +32,12 @@
 // order with strict '<' (lowest index on ties).  Every other candidate has
 // exact distance >= (second best, untagged) + |y|^2 - E; unless that bound
 // clears the best direct value by the fp32 error margins, the warp rescans
-// the whole row in the direct form.  So every code is the direct-form fp32
-// argmin wherever that differs from the exact one, as in encode.cu.
+// the whole row in the direct form.  The winner is then certified against
+// the rounding of the fp32 rotation and distances (code_certified); a row
+// that is not certified is decided again in float-float arithmetic by the
+// whole warp (nearest_exact, one or two in 10^4 rows), so a code can differ
+// from the exact nearest centroid only where two squared distances agree to
+// about 1e-10 relative.
 #include <math.h>
 
 #include <type_traits>
@@ -73,10 +77,13 @@ __device__ __forceinline__ const float *smooth_row(const EncodeParams &p, int64_
 }
 
 // Token v -> y = (1/sqrt D) H (s (.) x) (keys) or y = x (values), into yv.
+// Returns this lane's part of sum_i |fl(x_i s_i)| (keys; 0 for values), the
+// size of the rotation's rounding error.
 template <int E>
-__device__ __forceinline__ void forward_token(const EncodeParams &p, int64_t v, float inv_sqrt_d,
-                                              int lane, float *yv) {
+__device__ __forceinline__ float forward_token(const EncodeParams &p, int64_t v, float inv_sqrt_d,
+                                               int lane, float *yv) {
     float f[E];
+    float asum = 0.f;
     if (v < p.n_vec) {
         load_halves<E>(p.x + v * p.D + lane * E, f);
         if (p.rotate) {
@@ -87,7 +94,10 @@ __device__ __forceinline__ void forward_token(const EncodeParams &p, int64_t v, 
                 for (int j = 0; j < E; ++j) f[j] *= s[j];
             }
 #pragma unroll
-            for (int j = 0; j < E; ++j) f[j] *= inv_sqrt_d;
+            for (int j = 0; j < E; ++j) {
+                asum += fabsf(f[j]);
+                f[j] *= inv_sqrt_d;
+            }
             reg_fwht<E>(f, lane);
         }
     } else {
@@ -95,6 +105,7 @@ __device__ __forceinline__ void forward_token(const EncodeParams &p, int64_t v, 
         for (int j = 0; j < E; ++j) f[j] = 0.f;
     }
     store_floats<E>(yv + lane * E, f);
+    return asum;
 }
 
 // Chosen centroids in yv -> s^-1 (.) Hn y_hat (keys) or y_hat (values), fp16.
@@ -256,6 +267,9 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
     // packed codes (CodeT = uint32_t): the tile's token rows, assembled here
     constexpr bool kPacked = std::is_same<CodeT, uint32_t>::value;
     uint32_t *ptile = reinterpret_cast<uint32_t *>(misc + 4);
+    // rotation error bound of every token of the tile (<= 128 tokens)
+    float *delta_s = reinterpret_cast<float *>(ptile + 768);
+    const float dcoef = rotation_delta_coef(p.log2D, inv_sqrt_d);
 
     if (tid == 0) { misc[0] = 0.f; *bad_cb = 0; }
     for (int i = tid; i < npad * SUBD; i += kThr)
@@ -320,13 +334,17 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
         // ---- 1. load, smooth, rotate: one warp per token, in registers
         for (int t = warp; t < tok; t += kThr / 32) {
             float *yv = y_s + t * D;
+            float asum;
             switch (D) {
-                case 32: forward_token<1>(p, v0 + t, inv_sqrt_d, lane, yv); break;
-                case 64: forward_token<2>(p, v0 + t, inv_sqrt_d, lane, yv); break;
-                case 128: forward_token<4>(p, v0 + t, inv_sqrt_d, lane, yv); break;
-                case 256: forward_token<8>(p, v0 + t, inv_sqrt_d, lane, yv); break;
-                default: forward_token<16>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 32: asum = forward_token<1>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 64: asum = forward_token<2>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 128: asum = forward_token<4>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                case 256: asum = forward_token<8>(p, v0 + t, inv_sqrt_d, lane, yv); break;
+                default: asum = forward_token<16>(p, v0 + t, inv_sqrt_d, lane, yv); break;
             }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, off);
+            if (lane == 0) delta_s[t] = asum * dcoef;
         }
         if constexpr (kPacked) {
             for (int i = tid; i < tok * p.row_words; i += kThr) ptile[i] = 0u;
@@ -431,8 +449,9 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
             //     (its lane's two columns of every n-tile of its block), in
             //     increasing index order, strict '<': lowest index on ties
             const int pr = (c4 >> 1) * 16 + g + (c4 & 1) * 8;   // this lane's row
+            const float delta = delta_s[(R0 + pr) >> lsub];
             int code;
-            bool amb;
+            bool amb, cert;
             {
                 float y[SUBD];
                 load_floats<SUBD>(y_s + (R0 + pr) * SUBD, y);
@@ -443,13 +462,14 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                 const int nb = (int)(tg >> 2) * kBlockCols + 2 * (int)(tg & 3);
                 const int sb = cslot(nb);   // slots of nb + 8 j + col: (sb + 8 j) ^ col
                 // padding candidates (index >= N) sit at kFarCoord: d >= kFarDist
-                float b = INFINITY;
+                float b = INFINITY, b2 = INFINITY;   // best and second best of the group
                 int bj = 0;
 #pragma unroll
                 for (int j = 0; j < kBlockCols / 8; ++j) {
 #pragma unroll
                     for (int col = 0; col < 2; ++col) {
                         const float d = pair_dist<SUBD>(y2, cb_s + ((sb + j * 8) ^ col) * SUBD);
+                        b2 = fminf(b2, fmaxf(b, d));
                         if (d < b) { b = d; bj = 8 * j + col; }
                     }
                 }
@@ -468,6 +488,18 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                 amb = live && (cb_bad || !(ny2 <= kRange * kRange) || !(b < kFarDist) ||
                                !(outside - b > margin));
                 code = bi;
+                // lower bound on every other candidate's exact distance to y~:
+                // the group's second best, and the screen's bound for the
+                // other groups (its own rounding and that of |y|^2 included)
+                const float out_lb = outside - (E + tag_rel * fabsf(r2) +
+                                                 (float)(SUBD + 8) * kU * (fabsf(r2) + ny2));
+                cert = !live || amb || code_certified<SUBD>(b, fminf(b2, out_lb), delta);
+                // only the screen's bound is too loose: the direct rescan below
+                // gives every candidate's fp32 distance, then certify again
+                if (!cert && code_certified<SUBD>(b, b2, delta)) {
+                    amb = true;
+                    cert = true;
+                }
             }
             // (e) ambiguous rows: the whole warp rescans the row in the direct form
             {
@@ -478,19 +510,40 @@ encode_mma_kernel(EncodeParams p, float inv_sqrt_d, int npad) {
                     const int sc = src & 3;
                     const int spr = (sc >> 1) * 16 + (src >> 2) + (sc & 1) * 8;
                     const float *yr = y_s + (R0 + spr) * SUBD;
-                    float best = INFINITY;
+                    float best = INFINITY, second = INFINITY;
                     int bi = 0x7fffffff;
                     for (int n = lane; n < N; n += 32) {
                         const float d = direct_dist<SUBD>(yr, cb_s + cslot(n) * SUBD);
+                        second = fminf(second, fmaxf(best, d));
                         if (d < best) { best = d; bi = n; }
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
                         const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+                        const float os = __shfl_xor_sync(0xffffffffu, second, off);
                         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                        second = fminf(fminf(second, os), fmaxf(best, ob));
                         if (ob < best || (ob == best && oi < bi)) { best = ob; bi = oi; }
                     }
-                    if (lane == src) code = bi == 0x7fffffff ? 0 : bi;
+                    if (lane == src) {
+                        code = bi == 0x7fffffff ? 0 : bi;
+                        cert = code_certified<SUBD>(best, second, delta);
+                    }
+                }
+            }
+            // (e') rows the fp32 arithmetic cannot certify: float-float, whole warp
+            {
+                unsigned m = __ballot_sync(0xffffffffu, !cert);
+                while (m) {
+                    const int src = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int sc = src & 3;
+                    const int sl = R0 + (sc >> 1) * 16 + (src >> 2) + (sc & 1) * 8;
+                    const int cx = nearest_exact_token<SUBD>(
+                        p, v0 + (sl >> lsub), sl & (n_sub - 1),
+                        [cb_s](int c, int t) { return cb_s[cslot(c) * SUBD + t]; },
+                        delta_s[sl >> lsub], lane);
+                    if (lane == src) code = cx;
                 }
             }
             // (f) lane l takes the code of row l (held by quad lane q of quad
@@ -547,7 +600,8 @@ size_t mma_smem_bytes(int npad) {
     return sizeof(float) * (size_t)npad * SUBD + sizeof(uint2) * (size_t)(npad / 8) * C::KS * 32 +
            sizeof(float) * (size_t)kSlots * SUBD +
            sizeof(uint32_t) * (size_t)(kThr / 32) * kPassRows * C::AST + 16 +
-           sizeof(uint32_t) * 768;   // packed token rows of a tile (<= 512 / n_sub x words)
+           sizeof(uint32_t) * 768 +  // packed token rows of a tile (<= 512 / n_sub x words)
+           sizeof(float) * 128;      // rotation error bound per token (<= 512 / n_sub tokens)
 }
 
 template <int SUBD, typename CodeT>

@@ -221,6 +221,220 @@ __device__ __forceinline__ int token_head(const EncodeParams &p, int64_t v) {
     }
     return (int)((v / p.S) % p.H);
 }
+// ---------------------------------------------------------------- certified codes
+// The encode kernels decide in fp32.  A code is kept only when a rigorous
+// bound shows that it is the exact nearest centroid of the exact rotated
+// sub-vector y = Hn (s (.) x); otherwise it is decided again in float-float
+// arithmetic (nearest_exact: about 44 significant bits), so that a code can
+// differ from an exact (or float64) decision only where two squared
+// distances agree to about 1e-10 relative.  Error model (u = 2^-24):
+//   * the fp32 rotation: every element of y~ is within
+//       delta = (log2 D + 3) u sum_i |x_i s_i| / sqrt D
+//     of y (one rounding per butterfly stage, gamma_L <= (L + 3) u with the
+//     smooth product and the 1/sqrt D factor; delta = 0 without rotation);
+//     so | |y~ - c| - |y - c| | <= Delta = sqrt(sub_dim) delta for every c;
+//   * an fp32 squared distance of y~ (subtract, multiply-add chain) is within
+//     a relative (sub_dim + 4) u of the exact |y~ - c|^2.
+// With b an upper bound on the chosen centroid's |y~ - c|^2 and lo a lower
+// bound on every other centroid's, the choice is exact when
+//   sqrt(lo) - Delta > sqrt(b) + Delta.
+constexpr float kEncU = 5.9604645e-8f;   // 2^-24
+
+// delta per unit of sum_i |fl(x_i s_i)| (slack 1.002 covers the fp32 sum of
+// those terms, the rounding of 1/sqrt D and of the bound itself)
+__device__ __forceinline__ float rotation_delta_coef(int log2D, float inv_sqrt_d) {
+    return (float)(log2D + 3) * kEncU * 1.002f * inv_sqrt_d;
+}
+
+// sqrt(SUBD), rounded up
+template <int SUBD>
+struct SqrtSub {
+    static constexpr float v = SUBD == 1 ? 1.f : SUBD == 2 ? 1.4142136f : SUBD == 4 ? 2.f
+                             : SUBD == 8 ? 2.8284272f : 4.f;
+};
+
+// true when the fp32 decision is certified exact (see above): b and lo are
+// the fp32-computed values bounding the winner and the others
+template <int SUBD>
+__device__ __forceinline__ bool code_certified(float b, float lo, float delta) {
+    constexpr float gdir = (float)(SUBD + 4) * kEncU * 1.01f;
+    if (!(lo < INFINITY)) return b < INFINITY;   // no other candidate
+    const float ub = b * (1.f + gdir);
+    const float lb = lo * (1.f - gdir);
+    if (!(lb > 0.f) || !(ub >= 0.f)) return false;
+    const float two_delta = 2.004f * SqrtSub<SUBD>::v * delta;   // 2 Delta with rounding slack
+    // sqrt(lb) - sqrt(ub) >= (lb - ub) / (2 sqrt(lb)) >= (lb - ub) / (lb + 1):
+    // a sufficient test without square roots, then the exact one
+    if ((lb - ub) * (1.f - 4.f * kEncU) > two_delta * (lb + 1.f) * (1.f + 4.f * kEncU))
+        return true;
+    return sqrtf(lb) * (1.f - 4.f * kEncU) - sqrtf(ub) * (1.f + 4.f * kEncU) > two_delta;
+}
+
+// Float-float numbers hi + lo (|lo| <= ulp(hi) / 2 after normalisation),
+// from the error-free transformations TwoSum (Knuth, "The Art of Computer
+// Programming" vol. 2, 4.2.2) and the FMA form of TwoProduct.  Each
+// operation keeps about 44 significant bits.
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
+    const float s = a + b;
+    return {s, b - (s - a)};
+}
+__device__ __forceinline__ FF ff_two_prod(float a, float b) {
+    const float p = a * b;
+    return {p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const FF s = ff_two_sum(a.hi, b.hi);
+    return ff_fast_two_sum(s.hi, s.lo + (a.lo + b.lo));
+}
+__device__ __forceinline__ FF ff_mul(FF a, FF c) {
+    const FF p = ff_two_prod(a.hi, c.hi);
+    return ff_fast_two_sum(p.hi, fmaf(a.hi, c.lo, fmaf(a.lo, c.hi, p.lo)));
+}
+__device__ __forceinline__ bool ff_less(FF a, FF b) {
+    return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+// 1/sqrt(32 E) as a float-float constant (from the decimal value of the
+// mathematical constant; exact for E = 2, 8)
+template <int E>
+struct InvSqrtD {
+    static constexpr double v = E == 1 ? 0.17677669529663688110 : E == 2 ? 0.125
+                              : E == 4 ? 0.08838834764831844055 : E == 8 ? 0.0625
+                                       : 0.04419417382415922028;
+    static constexpr float hi = (float)v;
+    static constexpr float lo = (float)(v - (double)hi);
+};
+
+// Nearest centroid of sub-vector m of one token in float-float arithmetic,
+// by the whole warp (every lane returns it).  xv: the token's D = 32 E fp16
+// inputs; sm: its smooth factors or null; cent(c, t): coordinate t of
+// centroid c (fp32); delta: the token's fp32 rotation bound (above).  y is
+// recomputed from the fp16 input: each element is the signed sum over the
+// token of x_i s_i ((-1)^popc(r & i), the natural-order Sylvester sign) times
+// 1/sqrt D; without rotation y = x.  Distances in the direct form
+// sum_t (y_t - c_t)^2, the lowest index on ties (non-finite inputs: code 0).
+template <int SUBD, int E, typename Cent>
+__device__ __forceinline__ int nearest_exact_e(const __half *xv, const float *sm, int rotate,
+                                               Cent cent, int N, int m, float delta, int lane) {
+    FF y[SUBD];
+    if (rotate) {
+        // lane holds elements [E lane, E lane + E): all loads issued together
+        float xf[E], sf[E];
+        load_halves<E>(xv + lane * E, xf);
+        if (sm) {
+            load_floats<E>(sm + lane * E, sf);
+        } else {
+#pragma unroll
+            for (int j = 0; j < E; ++j) sf[j] = 1.f;
+        }
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) y[t] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            const int i = lane * E + j;
+            const FF xs = ff_two_prod(xf[j], sf[j]);   // x_i s_i exactly
+#pragma unroll
+            for (int t = 0; t < SUBD; ++t) {
+                const bool neg = __popc((m * SUBD + t) & i) & 1;
+                y[t] = ff_add(y[t], neg ? FF{-xs.hi, -xs.lo} : xs);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                y[t] = ff_add(y[t], FF{__shfl_xor_sync(0xffffffffu, y[t].hi, off),
+                                       __shfl_xor_sync(0xffffffffu, y[t].lo, off)});
+            // one value for every lane (the butterfly sums may differ in the last bit)
+            y[t] = ff_mul(FF{__shfl_sync(0xffffffffu, y[t].hi, 0), __shfl_sync(0xffffffffu, y[t].lo, 0)},
+                          FF{InvSqrtD<E>::hi, InvSqrtD<E>::lo});
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) y[t] = {__half2float(xv[m * SUBD + t]), 0.f};
+    }
+    // Candidates that can win: a screen in fp32 from yr = y.hi, within
+    // Delta_r = sqrt(SUBD) (u max|y| + delta) of y in the Euclidean norm
+    // (delta bounds the float-float sum's error many times over); fp32
+    // distances are within a relative (SUBD + 4) u.  Only candidates whose
+    // lower bound reaches the smallest upper bound are evaluated exactly.
+    float yr[SUBD];
+    float ymax = 0.f;
+#pragma unroll
+    for (int t = 0; t < SUBD; ++t) {
+        yr[t] = y[t].hi;
+        ymax = fmaxf(ymax, fabsf(yr[t]));
+    }
+    constexpr float g = (float)(SUBD + 4) * kEncU * 1.01f;
+    const float dr = SqrtSub<SUBD>::v * (ymax * kEncU + delta) * 1.01f;
+    auto d32 = [&](int c) {
+        float d = 0.f;
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) {
+            const float e = yr[t] - cent(c, t);
+            d = fmaf(e, e, d);
+        }
+        return d;
+    };
+    float dmin = INFINITY;
+    for (int c = lane; c < N; c += 32) dmin = fminf(dmin, d32(c));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dmin = fminf(dmin, __shfl_xor_sync(0xffffffffu, dmin, off));
+    // candidate c survives when sqrt(d32 (1 - g)) - dr <= sqrt(dmin (1 + g)) + dr
+    const float reach = (sqrtf(dmin * (1.f + g)) + 2.f * dr) * (1.f + 4.f * kEncU);
+    const float reach2 = reach * reach * (1.f + 4.f * kEncU);
+    FF best = {INFINITY, 0.f};
+    int bi = 0x7fffffff;
+    for (int c = lane; c < N; c += 32) {
+        if (!(d32(c) * (1.f - g) <= reach2)) continue;   // cannot be the nearest
+        FF acc = {0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < SUBD; ++t) {
+            const FF s = ff_two_sum(y[t].hi, -cent(c, t));
+            const FF e = ff_fast_two_sum(s.hi, s.lo + y[t].lo);
+            const FF q = ff_two_prod(e.hi, e.hi);
+            acc = ff_add(acc, ff_fast_two_sum(q.hi, fmaf(2.f * e.hi, e.lo, q.lo)));
+        }
+        if (ff_less(acc, best)) { best = acc; bi = c; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const FF ob = {__shfl_xor_sync(0xffffffffu, best.hi, off),
+                       __shfl_xor_sync(0xffffffffu, best.lo, off)};
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ff_less(ob, best) || (ob.hi == best.hi && ob.lo == best.lo && oi < bi)) {
+            best = ob;
+            bi = oi;
+        }
+    }
+    return bi == 0x7fffffff ? 0 : bi;
+}
+
+// nearest_exact_e for sub-vector m of token v of an encode call.
+template <int SUBD, typename Cent>
+__device__ __forceinline__ int nearest_exact_token(const EncodeParams &p, int64_t v, int m,
+                                                   Cent cent, float delta, int lane) {
+    const float *sm = !p.rotate || p.smooth_mode == 0 ? nullptr
+                      : p.smooth_mode == 2 ? p.smooth + (size_t)token_head(p, v) * p.D
+                                           : p.smooth;
+    const __half *xv = p.x + v * p.D;
+    switch (p.D) {
+        case 32: return nearest_exact_e<SUBD, 1>(xv, sm, p.rotate, cent, p.N, m, delta, lane);
+        case 64: return nearest_exact_e<SUBD, 2>(xv, sm, p.rotate, cent, p.N, m, delta, lane);
+        case 128: return nearest_exact_e<SUBD, 4>(xv, sm, p.rotate, cent, p.N, m, delta, lane);
+        case 256: return nearest_exact_e<SUBD, 8>(xv, sm, p.rotate, cent, p.N, m, delta, lane);
+        default: return nearest_exact_e<SUBD, 16>(xv, sm, p.rotate, cent, p.N, m, delta, lane);
+    }
+}
+
 // Returns a cudaError_t of the launch.
 cudaError_t launch_encode(const EncodeParams &p, cudaStream_t stream);
 size_t encode_smem_bytes(int N, int sub_dim);

@@ -13,17 +13,6 @@ def dev(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def smooth_rows(smooth, shape):
-    """Smooth factor of every element of a [B, H, S, D] tensor, [n, D]."""
-    B, H, S, D = shape
-    if smooth is None:
-        return None
-    s = np.asarray(smooth, np.float64)
-    if s.ndim == 1:
-        s = np.broadcast_to(s, (H, D))
-    return np.broadcast_to(s[None, :, None, :], shape).reshape(-1, D)
-
-
 def check_encode(x16, codebook, sub_dim, smooth, rotate, gpu_codes, gpu_hat,
                  rows=None):
     """Oracle-check codes (and the fp16 reconstruction) of x16 [B, H, S, D].
@@ -35,7 +24,6 @@ def check_encode(x16, codebook, sub_dim, smooth, rotate, gpu_codes, gpu_hat,
     n = B * H * S
     xf = x16.reshape(n, D)
     heads = np.broadcast_to(np.arange(H)[None, :, None], (B, H, S)).reshape(n)
-    srows = smooth_rows(smooth, x16.shape) if rotate else None
     if rows is None:
         rows = np.arange(n)
     rows = np.asarray(rows)
@@ -43,9 +31,7 @@ def check_encode(x16, codebook, sub_dim, smooth, rotate, gpu_codes, gpu_hat,
                       smooth=smooth if rotate else None, rotate=rotate,
                       want_y=True, want_xhat=gpu_hat is not None)
     g = gpu_codes.reshape(n, -1)[rows].astype(np.int64)
-    res = parity.check_codes(g, o, x=xf[rows].astype(np.float64),
-                             smooth_rows=None if srows is None else srows[rows],
-                             rotate=rotate, codebook=codebook)
+    res = parity.check_codes(g, o)
     if gpu_hat is not None:
         # compare the reconstruction where every code of the vector agrees;
         # vectors with a justified code difference are counted above
