@@ -1,12 +1,13 @@
 """Benchmark of the product-VQ KV-cache hot path on GB300.
 
-Default workload (N=1): single-sequence decode -- encode 8192 new keys of
-B=1, H=8, D=128 (uint8 codes, 256x4 codebook) and attend one query per head
-over the 8192 coded keys (values pre-encoded outside the timed region).
-One step = vq_encode_keys + vq_decode_attend (+ its combine pass).
+Default workload (N=1): batched GQA decode -- B=32 sequences, H_q=32 query
+heads over H_kv=8 KV heads, D=128, one query token each attending over
+S_kv=32768 coded keys (uint8 K and V codes, 256x4 codebooks).  One step =
+vq_decode_attend (the split-KV kernel + its combine pass).
 
-Other workloads (--workload): gqa-decode, gqa-decode-ragged, decode-append,
-bulk-encode, bulk-encode-packed, chunked-prefill.
+Other workloads (--workload): decode-1seq (encode 8192 new keys + attend),
+gqa-decode-ragged, decode-append, bulk-encode, bulk-encode-packed,
+chunked-prefill.
 
 Prints ONE JSON line (rank 0).  `value` is device-timed throughput with
 inputs resident in HBM; `e2e` repeats the step through the same C-ABI calls
@@ -14,7 +15,11 @@ from pinned host buffers with the host<->device copies inside the timed
 region.  L2 is flushed (a 256 MiB write) before every timed step.
 
 --impl reference times the float64 CPU oracle on a bounded sample of the
-same workload (the CPU baseline); under torchrun only rank 0 runs it.
+same workload (the CPU baseline) on all host cores; under torchrun only
+rank 0 runs it.  The GPU line's cpu_baseline reports the same oracle on one
+thread and on all host cores, and `parity` compares the oracle's results on
+that sample with the GPU step's (code mismatches / near ties, or the
+attention rows' max error).
 """
 from __future__ import annotations
 
@@ -412,94 +417,153 @@ def run_gpu(args, name, rank, world):
         "wall_s_timed_region": round(wall, 4), "output_finite": finite,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(name, spec, inp, budget_s=args.cpu_budget)
+        gpu_out = {}
+        if name in ("decode-1seq", "bulk-encode"):
+            gpu_out["k_codes"] = r.d["k_codes"].cpu().numpy()
+        elif not name.startswith("bulk-encode"):
+            gpu_out["out"] = r.d["out"].float().cpu().numpy()
+        cb = cpu_baseline(name, spec, inp, budget_s=args.cpu_budget, gpu=gpu_out)
+        line["parity"] = cb.pop("parity", None)
+        line["cpu_baseline"] = cb
     return line
 
 
 # ------------------------------------------------------------- CPU arm (oracle)
 
-def cpu_baseline(name, spec, inp, budget_s=15.0):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _concurrent_wall(fn, args_list):
+    """Wall seconds to run fn over args_list on one thread each (the oracle
+    is C behind ctypes, which releases the GIL: the threads run in parallel)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=len(args_list)) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(fn, args_list))
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(name, spec, inp, budget_s=10.0, gpu=None):
     """Time the float64 oracle, as it stands, on a bounded sample of the
-    workload and scale it to the metric's unit (one thread)."""
+    workload and scale it to the metric's unit: once on one thread and once
+    on every host core (threads over disjoint parts of the sample).  With
+    ``gpu`` (the GPU step's outputs as numpy arrays) the oracle's results on
+    the sample are also compared with the GPU's (the parity counts)."""
     import oracle
+    from oracle import parity as par
     oracle.build()
     D = spec.D
-    rng = np.random.default_rng(0)
+    cores = host_cores()
+    n_bg = spec.B * spec.H_kv
+    n_rows = spec.B * spec.H_q * spec.S_q
+    report = {}
 
-    def time_encode(n_vec):
+    def encode_sample(seed, n_vec):
         keys = inp["keys"].reshape(-1, D)
         heads = np.broadcast_to(np.arange(spec.H_kv)[None, :, None],
                                 inp["keys"].shape[:3]).reshape(-1)
-        idx = rng.integers(0, keys.shape[0], n_vec)
+        idx = np.random.default_rng(seed).integers(0, keys.shape[0], n_vec)
         t0 = time.perf_counter()
-        oracle.encode(keys[idx], inp["k_codebook"], heads=heads[idx], smooth=inp["smooth"])
-        return time.perf_counter() - t0
+        out = oracle.encode(keys[idx], inp["k_codebook"], heads=heads[idx], smooth=inp["smooth"])
+        return time.perf_counter() - t0, idx, out
 
-    def time_attend(n_rows):
-        """Oracle attention of n_rows rows of one (batch, kv head): the
+    def attend_sample(pair, n_rows_s):
+        """Oracle attention of n_rows_s rows of one (batch, kv head): the
         K_hat reconstruction of that head plus the rows."""
+        b, g = divmod(pair % n_bg, spec.H_kv)
         if "k_codes" in inp:
-            kc, vc = inp["k_codes"][:1, :1], inp["v_codes"][:1, :1]
+            kc, vc = inp["k_codes"][b:b + 1, g:g + 1], inp["v_codes"][b:b + 1, g:g + 1]
         else:
-            kc = rng.integers(0, spec.k_N, (1, 1, spec.S_kv, spec.n_k))
-            vc = rng.integers(0, spec.v_N, (1, 1, spec.S_kv, spec.n_v))
+            r = np.random.default_rng(pair)
+            kc = r.integers(0, spec.k_N, (1, 1, spec.S_kv, spec.n_k))
+            vc = r.integers(0, spec.v_N, (1, 1, spec.S_kv, spec.n_v))
+        if "kv_lens" in inp:
+            L = int(inp["kv_lens"][b])
+            kc, vc = kc[:, :, :L], vc[:, :, :L]
         rows = np.array([[0, r % spec.G, spec.S_q - 1 - (r // spec.G) % spec.S_q]
-                         for r in range(n_rows)])
+                         for r in range(n_rows_s)])
+        q = inp["q"][b:b + 1, g * spec.G:(g + 1) * spec.G]
+        sm = None if inp["smooth"] is None else inp["smooth"][g:g + 1]
         t0 = time.perf_counter()
-        oracle.attend_rows(inp["q"][:1, :spec.G], kc, inp["k_codebook"], vc,
-                           inp["v_codebook"], None if inp["smooth"] is None else inp["smooth"][:1],
-                           spec.sm_scale, spec.causal, spec.window, rows)
-        return time.perf_counter() - t0
+        out = oracle.attend_rows(q, kc, inp["k_codebook"], vc, inp["v_codebook"], sm,
+                                 spec.sm_scale, spec.causal, spec.window, rows)
+        return time.perf_counter() - t0, (b, g, rows), out
 
-    def attend_model():
-        t1, t5 = time_attend(1), time_attend(5)
+    def attend_model(pair):
+        t1 = attend_sample(pair, 1)[0]
+        t5, where, out = attend_sample(pair, 5)
         per_row = max((t5 - t1) / 4, 0.0)
-        per_head = max(t1 - per_row, 0.0)
-        return per_head, per_row
+        return max(t1 - per_row, 0.0), per_row, t1 + t5, where, out
 
-    n_bg = spec.B * spec.H_kv
-    n_rows = spec.B * spec.H_q * spec.S_q
+    def attend_parity(where, out):
+        if gpu is None or "out" not in gpu:
+            return
+        b, g, rows = where
+        got = np.stack([gpu["out"][b, g * spec.G + h, i] for _, h, i in rows]).astype(np.float64)
+        ok, err, _ = par.allclose_report(got, oracle.to_f16(out).astype(np.float64))
+        report["parity"] = {"attention_rows": int(len(rows)), "max_abs_err": err,
+                            "tolerance": "2e-3 + 1e-2 |ref|", "ok": ok}
+
     if name in ("decode-1seq", "bulk-encode", "bulk-encode-packed"):
         n_total = spec.B * spec.H_kv * spec.enc_len
-        per = time_encode(64) / 64
-        n_s = int(max(64, min(n_total, 0.6 * budget_s / max(per, 1e-9))))
-        full = time_encode(n_s) * n_total / n_s
-        sample = f"oracle key encode of {n_s} of {n_total} vectors, scaled"
+        per = encode_sample(0, 64)[0] / 64
+        n_s = int(max(64, min(n_total, 0.5 * budget_s / max(per, 1e-9))))
+        t1, idx, out = encode_sample(1, n_s)
+        wall = _concurrent_wall(lambda k: encode_sample(2 + k, n_s), list(range(cores)))
+        full1 = t1 * n_total / n_s
+        fullN = wall * n_total / (n_s * cores)
+        sample = f"oracle key encode of {n_s} of {n_total} vectors (per thread), scaled"
+        if gpu is not None and "k_codes" in gpu:
+            res = par.check_codes(gpu["k_codes"].reshape(n_total, -1)[idx].astype(np.int64), out)
+            report["parity"] = {"codes": res}
         if name == "decode-1seq":
-            per_head, per_row = attend_model()
-            full += n_bg * per_head + n_rows * per_row
+            ph, pr, tt, _, _ = attend_model(0)
+            wall = _concurrent_wall(attend_model, list(range(cores)))
+            full1 += n_bg * ph + n_rows * pr
+            fullN += (n_bg * ph + n_rows * pr) * wall / (cores * tt)
             sample += (f"; oracle attention of 1 and 5 rows of one kv head over "
                        f"{spec.S_kv} keys, scaled to {n_bg} heads and {n_rows} rows")
-            value = spec.B * spec.S_q / full
+            value1, valueN = spec.B * spec.S_q / full1, spec.B * spec.S_q / fullN
         else:
-            value = n_total / full
+            value1, valueN = n_total / full1, n_total / fullN
     else:
-        per_head, per_row = attend_model()
+        ph, pr, tt, where, out = attend_model(0)
+        attend_parity(where, out)
+        wall = _concurrent_wall(attend_model, list(range(cores)))
         # per-batch cache lengths: both costs scale with the keys attended
         frac = float(np.mean(inp["kv_lens"])) / spec.S_kv if "kv_lens" in inp else 1.0
-        full = (n_bg * per_head + n_rows * per_row) * frac
+        full1 = (n_bg * ph + n_rows * pr) * frac
+        fullN = full1 * wall / (cores * tt)
         sample = (f"oracle attention of 1 and 5 rows of one (batch, kv head) over "
-                  f"{spec.S_kv} keys, scaled to {n_bg} pairs and {n_rows} rows")
+                  f"{spec.S_kv} keys (per thread), scaled to {n_bg} pairs and {n_rows} rows")
         if frac != 1.0:
             sample += f" and by the mean cache length ({frac:.3f} of S_kv)"
         if name == "decode-append":
             n_new = spec.B * spec.H_kv * spec.enc_len
-            full += time_encode(n_new)
+            t_enc = encode_sample(0, n_new)[0]
             t0 = time.perf_counter()
             oracle.encode(inp["values"].reshape(-1, D), inp["v_codebook"], rotate=False)
-            full += time.perf_counter() - t0
+            t_enc += time.perf_counter() - t0
+            full1 += t_enc
+            fullN += t_enc   # a handful of vectors: not split across threads
             sample = f"oracle key and value encode of the {n_new} new vectors; " + sample
-        value = spec.B * spec.S_q / full
-    return {"value": value, "unit": METRICS[name][1], "cores": 1, "kind": "oracle",
-            "sample": sample, "est_step_s": full}
+        value1, valueN = spec.B * spec.S_q / full1, spec.B * spec.S_q / fullN
+    report.update({"value": valueN, "unit": METRICS[name][1], "cores": cores,
+                   "kind": "oracle", "sample": sample, "est_step_s": fullN,
+                   "single_core": {"value": value1, "cores": 1, "est_step_s": full1}})
+    return report
 
 
 def run_reference(args, name):
     spec = WORKLOADS[name]
     inp = make_inputs(spec)
     vals = []
-    for _ in range(args.warmup):
-        cpu_baseline(name, spec, inp, budget_s=2.0)
+    for _ in range(min(args.warmup, 1)):
+        cpu_baseline(name, spec, inp, budget_s=1.0)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         vals.append(cpu_baseline(name, spec, inp, budget_s=args.cpu_budget / max(1, args.steps)))
@@ -525,8 +589,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode-1seq", choices=sorted(METRICS))
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--workload", default="gqa-decode", choices=sorted(METRICS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))

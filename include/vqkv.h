@@ -90,9 +90,13 @@ VQ_API const char *vq_status_str(int status);
  *
  * Per vector x of head h: y = Hn (s_h (.) x) with Hn the normalised
  * Sylvester-Hadamard matrix; code_m = the nearest centroid of sub-vector
- * y[m*sub_dim : (m+1)*sub_dim] by squared Euclidean distance in fp32, the
- * lowest index on ties; k_hat = s_h^-1 (.) Hn concat_m codebook[code_m],
- * rounded to fp16 (nearest even).
+ * y[m*sub_dim : (m+1)*sub_dim] by squared Euclidean distance, the lowest
+ * index on ties; k_hat = s_h^-1 (.) Hn concat_m codebook[code_m], rounded to
+ * fp16 (nearest even).  The search runs in fp32; a decision that a rigorous
+ * bound on the fp32 rounding (of y and of the distances) cannot certify is
+ * taken again in float-float arithmetic (about 44 significant bits), so a
+ * code differs from the exact nearest centroid of the exact y only where
+ * two squared distances agree to about 1e-10 relative.
  *
  * Errors: VQ_ERR_NULL (keys, codebook, codes, or smooth when smooth_mode
  * != 0), VQ_ERR_SHAPE (a size < 0, D % sub_dim != 0, smooth_mode not in
@@ -112,8 +116,8 @@ VQ_API int vq_encode_keys(const void *keys_f16, int B, int H, int S, int D,
  * encoder without the smooth and Hadamard steps.
  *
  * Same arguments, limits and errors as vq_encode_keys without smooth: per
- * vector, code_m = nearest centroid of x[m*sub_dim : (m+1)*sub_dim] (fp32
- * squared distance, lowest index on ties); v_hat (optional) =
+ * vector, code_m = nearest centroid of x[m*sub_dim : (m+1)*sub_dim] (squared
+ * distance, lowest index on ties, decided as for keys); v_hat (optional) =
  * concat_m codebook[code_m] rounded to fp16.
  */
 VQ_API int vq_encode_values(const void *values_f16, int B, int H, int S, int D,
@@ -248,9 +252,9 @@ VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
  * accumulators in tensor memory).  Used when S_q >= 64; smaller S_q, or
  * shapes outside the tensor-core kernel's limits (D != 128, sub_dim != 4,
  * codes wider than one byte), are served by vq_decode_attend with the same
- * arguments.  An even GQA group size H_q / H_kv runs two query heads of a
- * KV group per block (sharing the rebuilt tiles); an odd one runs one head
- * per block.  Page: "Metal
+ * arguments.  Each block runs two query heads of a KV group (sharing the
+ * rebuilt tiles); with an odd GQA group size H_q / H_kv the last block of a
+ * group runs a single head.  Page: "Metal
  * Kernels API", section "Fused SDPA", metal_fused_sdpa; the prefill-shaped
  * tile loop follows the companion described under rabitq_prefill_attend.
  * Errors as vq_decode_attend.
@@ -270,15 +274,23 @@ VQ_API int vq_prefill_attend(const vq_attend_args *args, void *stream);
  * partial results go to a scratch array of VQ_NOALLOC_SCRATCH_BYTES compiled
  * into the library, which every GPU that loads the library keeps until the
  * process exits.  The library allocates nothing, here or anywhere.
- *   - A problem whose partial results do not fit the array even with a
- *     single key split returns VQ_ERR_WORKSPACE (larger problems otherwise
- *     run with fewer splits); use vq_decode_attend with a workspace for those.
+ *   - A problem fits exactly when
+ *       (B * H_kv * ceil(H_q / H_kv * S_q / 8) + 1) * 8 * (D + 4) * 4
+ *         <= VQ_NOALLOC_SCRATCH_BYTES
+ *     (its partial results with a single key split); problems whose regular
+ *     split (vq_attend_workspace_bytes) needs more than the array run with
+ *     fewer, longer splits.  A problem that does not fit returns
+ *     VQ_ERR_WORKSPACE before anything is launched; use vq_decode_attend
+ *     with a workspace for those.
  *   - All calls share the array: calls whose work overlaps on the GPU (other
  *     streams or host threads) race on it; order them on one stream or with
  *     events.  Every call overwrites what it reads, so no clearing is needed.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and keeps it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it with the
+ *     id of the device's context; make that first call before any stream
+ *     capture.  A call that finds another context current (after
+ *     cudaDeviceReset, or a primary context released and re-created) looks
+ *     the address up again: make that call outside a stream capture too.
  */
 #define VQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 VQ_API int vq_decode_attend_noalloc(const vq_attend_args *args, void *stream);

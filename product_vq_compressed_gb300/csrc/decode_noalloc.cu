@@ -22,7 +22,14 @@
 // names a stand-in object, not device memory), so the first call on each
 // device looks up the array's device address with cudaGetSymbolAddress while
 // that device is current and keeps it; make that first call before any
-// stream capture.  No allocation happens here at any time.
+// stream capture.  The address belongs to the device's context: it is kept
+// together with the context's unique id (cuCtxGetId, reached through
+// cudaGetDriverEntryPointByVersion, so the library needs no link to the
+// driver library), and looked up again when a call finds another context
+// current (after cudaDeviceReset, or when the host application released and
+// re-created the primary context).  No allocation happens here at any time.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "vq_internal.cuh"
@@ -35,22 +42,59 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+    void *addr;
+    unsigned long long ctx_id;   // 0: unknown
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once
-// per device).  Returns VQ_OK or VQ_ERR_CUDA.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_entry_once;
+
+// Unique id of the current context (never reused within the process), or 0
+// when there is no current context or the driver cannot tell.
+unsigned long long current_context_id() {
+    std::call_once(g_entry_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!g_ctx_get_current || !g_ctx_get_id || g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        g_ctx_get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current device's context
+// (looked up once per context).  Returns VQ_OK or VQ_ERR_CUDA.
 int scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return VQ_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchEntry &e = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (!e.addr || id == 0 || id != e.ctx_id) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
             return VQ_ERR_CUDA;
-        g_scratch_addr[dev] = ptr;
+        e.addr = ptr;
+        e.ctx_id = current_context_id();   // the lookup made the context current
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return VQ_OK;
 }
 
@@ -60,34 +104,13 @@ extern "C" {
 
 int vq_decode_attend_noalloc(const vq_attend_args *args, void *stream) {
     if (!args) return VQ_ERR_NULL;
-    // same validation as vq_decode_attend, without the caller's workspace
+    // the checks of vq_decode_attend, without the caller's workspace
     vq_attend_args a = vqkv::normalize_code_widths(*args);
     a.workspace = nullptr;
     a.workspace_bytes = 0;
-    if (a.B < 0 || a.H_q < 0 || a.H_kv < 0 || a.S_q < 0 || a.S_kv < 0 || a.D < 1 ||
-        a.sliding_window < 0 || a.H_kv == 0 || a.H_q % a.H_kv != 0 ||
-        a.k_sub_dim < 1 || a.v_sub_dim < 1 || a.D % a.k_sub_dim != 0 ||
-        a.D % a.v_sub_dim != 0 || a.smooth_mode < 0 || a.smooth_mode > 2 ||
-        ((a.causal || a.sliding_window > 0) && a.S_q > a.S_kv) ||
-        (a.S_kv == 0 && a.S_q > 0 && a.B > 0 && a.H_q > 0) ||
-        a.k_code_bytes < 0 || a.k_code_bytes > 2 || a.v_code_bytes < 0 || a.v_code_bytes > 2 ||
-        a.kv_stride < 0 || (a.kv_stride > 0 && a.kv_stride < a.S_kv))
-        return VQ_ERR_SHAPE;
-    if (a.k_n_centroids < 1 || a.v_n_centroids < 1 ||
-        a.k_n_centroids > (a.k_code_bytes == 1 ? 256 : 65536) ||
-        a.v_n_centroids > (a.v_code_bytes == 1 ? 256 : 65536) ||
-        (a.D & (a.D - 1)) != 0)
-        return VQ_ERR_UNSUPPORTED;
-    int rc = vqkv::decode_supported(a);
+    int rc = vqkv::attend_validate(&a);
     if (rc != VQ_OK) return rc;
     if ((int64_t)a.B * a.H_q * a.S_q == 0) return VQ_OK;
-    if (!a.q_f16 || !a.k_codes || !a.k_codebook || !a.v_codes || !a.v_codebook ||
-        !a.out_f16 || (a.smooth_mode != 0 && !a.smooth))
-        return VQ_ERR_NULL;
-    const void *ptrs[] = {a.q_f16, a.k_codes, a.k_codebook, a.v_codes,
-                          a.v_codebook, a.out_f16, a.smooth};
-    for (const void *p : ptrs)
-        if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return VQ_ERR_ALIGN;
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

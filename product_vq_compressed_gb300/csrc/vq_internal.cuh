@@ -458,6 +458,11 @@ struct DequantParams {
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- attend
+// Argument checks of the attention entry points (sizes, limits, pointers,
+// alignment; in the order include/vqkv.h states), VQ_OK or a status.  The
+// workspace size is checked by each entry point against its own plan.
+int attend_validate(const vq_attend_args *a);
+
 struct AttendPlan {
     int n_split;        // 1 (0 when a capped plan cannot fit)
     int cols;           // query columns (head, row) pairs per column block

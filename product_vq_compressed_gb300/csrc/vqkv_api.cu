@@ -74,7 +74,35 @@ int encode_common(const void *x, int B, int H, int S, int D,
                : VQ_ERR_CUDA;
 }
 
-// Shape checks shared by both attention entry points.
+int current_sms(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return VQ_ERR_CUDA;
+    return VQ_OK;
+}
+
+int decode_impl(const vq_attend_args *a, void *stream) {
+    int rc = vqkv::attend_validate(a);
+    if (rc != VQ_OK) return rc;
+    if ((int64_t)a->B * a->H_q * a->S_q == 0) return VQ_OK;
+    int sms = 0;
+    rc = current_sms(&sms);
+    if (rc != VQ_OK) return rc;
+    const vqkv::AttendPlan plan = vqkv::plan_decode(*a, sms);
+    if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return VQ_ERR_WORKSPACE;
+    return vqkv::launch_decode(*a, plan, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? VQ_OK
+               : VQ_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace vqkv {
+// Argument checks shared by every attention entry point (decode, prefill,
+// and the allocation-free decode); the workspace size is checked by the
+// caller, which knows its plan.
 int attend_validate(const vq_attend_args *a) {
     if (!a) return VQ_ERR_NULL;
     if (a->B < 0 || a->H_q < 0 || a->H_kv < 0 || a->S_q < 0 || a->S_kv < 0 ||
@@ -107,30 +135,7 @@ int attend_validate(const vq_attend_args *a) {
     return VQ_OK;
 }
 
-int current_sms(int *sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return VQ_ERR_CUDA;
-    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return VQ_ERR_CUDA;
-    return VQ_OK;
-}
-
-int decode_impl(const vq_attend_args *a, void *stream) {
-    int rc = attend_validate(a);
-    if (rc != VQ_OK) return rc;
-    if ((int64_t)a->B * a->H_q * a->S_q == 0) return VQ_OK;
-    int sms = 0;
-    rc = current_sms(&sms);
-    if (rc != VQ_OK) return rc;
-    const vqkv::AttendPlan plan = vqkv::plan_decode(*a, sms);
-    if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return VQ_ERR_WORKSPACE;
-    return vqkv::launch_decode(*a, plan, reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? VQ_OK
-               : VQ_ERR_CUDA;
-}
-
-}  // namespace
+}  // namespace vqkv
 
 extern "C" {
 
@@ -233,7 +238,7 @@ int vq_prefill_attend(const vq_attend_args *in, void *stream) {
     if (!in) return VQ_ERR_NULL;
     const vq_attend_args n = vqkv::normalize_code_widths(*in);
     const vq_attend_args *args = &n;
-    int rc = attend_validate(args);
+    int rc = vqkv::attend_validate(args);
     if (rc != VQ_OK) return rc;
     if (vqkv::prefill_supported(*args) != VQ_OK) return decode_impl(args, stream);
     if ((int64_t)args->B * args->H_q * args->S_q == 0) return VQ_OK;

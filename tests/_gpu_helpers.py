@@ -64,3 +64,39 @@ def run_attend(entry, inp, spec, k_codes, v_codes, causal=None, window=None):
               dev(inp["v_codebook"]), dev(inp["smooth"]), spec.sm_scale,
               causal=spec.causal if causal is None else causal,
               sliding_window=spec.window if window is None else window)
+
+
+def oracle_attend_rows_parallel(inp, spec, rows, k_codes, v_codes, workers=None):
+    """oracle_attend_rows for many rows of a full-size workload: the rows of
+    each (batch, KV head) go to the oracle with that head's slice of the
+    inputs only, one thread per (batch, KV head) (the C oracle releases the
+    GIL).  Per-batch cache lengths are applied by slicing the codes."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    rows = np.asarray(rows)
+    G = spec.G
+    groups = {}
+    for k, (b, h, i) in enumerate(rows):
+        groups.setdefault((int(b), int(h) // G), []).append(k)
+    out = np.zeros((len(rows), spec.D))
+    sm = inp["smooth"]
+
+    def one(key):
+        b, g = key
+        ks = groups[key]
+        kc, vc = k_codes[b:b + 1, g:g + 1], v_codes[b:b + 1, g:g + 1]
+        if "kv_lens" in inp:
+            L = int(inp["kv_lens"][b])
+            kc, vc = kc[:, :, :L], vc[:, :, :L]
+        local = np.array([[0, rows[k, 1] - g * G, rows[k, 2]] for k in ks])
+        order = np.lexsort((local[:, 2], local[:, 1]))
+        res = oracle.attend_rows(
+            inp["q"][b:b + 1, g * G:(g + 1) * G], kc, inp["k_codebook"], vc,
+            inp["v_codebook"], None if sm is None else (sm if sm.ndim == 1 else sm[g:g + 1]),
+            spec.sm_scale, spec.causal, spec.window, local[order])
+        out[np.asarray(ks)[order]] = res
+
+    n = workers or min(len(groups), max(1, len(os.sched_getaffinity(0))))
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(one, list(groups)))
+    return out

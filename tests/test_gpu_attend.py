@@ -4,13 +4,14 @@ Both sides get the same codes (drawn uniformly, or encoded by the oracle),
 so the comparison isolates the attention kernel.  Outputs are fp16 and held
 to |err| <= 2e-3 + 1e-2 |ref|.  Small cases span several 16-key tiles, key
 splits and column blocks, with ragged tails; full-size workloads are checked
-on sampled rows.
+on sampled rows and on whole query tiles / whole GQA groups in the launch
+configuration the benchmark times.
 """
 import numpy as np
 import pytest
 import torch
 
-from _gpu_helpers import DEV, dev, oracle_attend_rows, run_attend
+from _gpu_helpers import DEV, dev, oracle_attend_rows, oracle_attend_rows_parallel, run_attend
 import oracle
 from oracle import parity
 from product_vq_compressed_gb300 import binding as vq
@@ -138,6 +139,45 @@ def test_attend_full_size_sampled(name, entry, n_bg, rows_per):
     rows.append((0, 0, spec.S_q - 1))
     err = _check(spec, inp, out, rows)
     print(name, entry, "rows", len(rows), "max |err|", err)
+
+
+def test_chunked_prefill_full_size_whole_tiles():
+    """Chunked prefill at full size through the tensor-core kernel (the
+    launch the benchmark times): every row of whole 128-row query tiles for
+    both heads of a CTA's head pair -- the first tile, the second, the last,
+    and a middle tile of the last KV group.  The sliding window's lower bound
+    cuts the first key tile of every query tile."""
+    spec = WORKLOADS["chunked-prefill"]
+    inp = make_inputs(spec)
+    out = run_attend("prefill", inp, spec, inp["k_codes"], inp["v_codes"])
+    torch.cuda.synchronize()
+    last = spec.S_q // 128 - 1
+    plan = [(0, (0, 1)), (1, (0, 1)), (last, (2, 3)), (7, (spec.H_q - 2, spec.H_q - 1))]
+    rows = np.array([(0, h, i) for t, hs in plan for h in hs
+                     for i in range(128 * t, 128 * t + 128)])
+    ref = oracle_attend_rows_parallel(inp, spec, rows, inp["k_codes"], inp["v_codes"])
+    got = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    ok, err, excess = parity.allclose_report(got, ref)
+    assert ok, f"max |err| {err}, worst excess {excess}"
+
+
+@pytest.mark.parametrize("name", ["gqa-decode", "gqa-decode-ragged"])
+def test_gqa_decode_full_size_whole_batches(name):
+    """Batched GQA decode at full size: all 32 query heads (every KV head's
+    group) of the first and the last batch."""
+    spec = WORKLOADS[name]
+    inp = make_inputs(spec)
+    kv_lens = inp.get("kv_lens")
+    out = vq.decode_attend(dev(inp["q"]), dev(inp["k_codes"]), dev(inp["k_codebook"]),
+                           dev(inp["v_codes"]), dev(inp["v_codebook"]), dev(inp["smooth"]),
+                           spec.sm_scale, causal=spec.causal, sliding_window=spec.window,
+                           kv_lens=dev(kv_lens))
+    torch.cuda.synchronize()
+    rows = np.array([(b, h, 0) for b in (0, spec.B - 1) for h in range(spec.H_q)])
+    ref = oracle_attend_rows_parallel(inp, spec, rows, inp["k_codes"], inp["v_codes"])
+    got = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    ok, err, excess = parity.allclose_report(got, ref)
+    assert ok, f"max |err| {err}, worst excess {excess}"
 
 
 def test_workspace_too_small_is_rejected():
