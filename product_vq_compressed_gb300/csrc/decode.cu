@@ -45,7 +45,7 @@ constexpr int kCols = 8;         // query columns per unit (MMA N)
 constexpr int kTile = 16;        // keys per MMA tile
 constexpr int kPrefetchTiles = 8;  // L2 prefetch distance
 constexpr int kPfKeys = 2 * kTile * 2;  // keys per prefetch: two steps of two tiles
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLog2e = 1.4426950408889634;
 constexpr float kSlack = 8.f;    // base-2 headroom of a column's reference maximum
 
 // ------------------------------------------------------------ primitives
@@ -232,8 +232,7 @@ struct DecArgs {
     int Nv;
     const float *smooth;
     int smooth_mode;
-    float sl;          // scale * log2(e)
-    float inv_sqrt_d;
+    float qscale;      // 1/sqrt(D) * scale * log2(e): applied to q~ (base-2 scores)
     int causal, window;
     int64_t stride;        // code rows per (b, kv head)
     const int32_t *kv_lens;  // keys held by each batch, or null (all S_kv)
@@ -345,6 +344,7 @@ struct UnitState {
     uint32_t bq[D / 16][2];
     float acc_o[D / 16][4];
     float m0, m1, l0, l1;
+    float mu0, mu1;             // exponent reference of the lane's two columns
     int lo0, hi0, lo1, hi1;     // bounds of the lane's two columns
     int lo_any, hi_any;         // keys every real column sees
     int lo_all, hi_all;         // keys some column sees
@@ -364,7 +364,10 @@ __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const 
     }
 }
 
-template <int D, int DK, int DV, bool FAST>
+// One 32-key step.  MASK: the step needs the per-column key bounds (the
+// first and last steps of a segment); the steps between take the unmasked
+// instantiation, in which every real column sees every key.
+template <int D, int DK, int DV, bool FAST, bool MASK>
 __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int j0,
                                              UnitState<D> &u, const DecArgs &a,
                                              uint32_t kbase, uint32_t vbase, int krow,
@@ -373,7 +376,7 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
                                              uint32_t vlane) {
     using SC = StepCodes<D, DK, DV>;
     constexpr int KSTEPS = D / 16, MT = D / 16;
-    if (j0 > u.hi_all || j0 + kStepKeys - 1 < u.lo_all) return;  // nobody sees it
+    if (MASK && (j0 > u.hi_all || j0 + kStepKeys - 1 < u.lo_all)) return;  // nobody sees it
 
     // ---- S^T = K~ Q~^T for both tiles; even / odd k-steps accumulate
     //      separately so the four MMA chains are independent
@@ -416,16 +419,16 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
             mma16816(s[t][ks & 1], f[t][0][0], f[t][1][0], f[t][0][1], f[t][1][1], u.bq[ks][0],
                      u.bq[ks][1]);
     }
-    // ---- scale, mask, online softmax for columns 2c4 and 2c4+1
+    // ---- mask, online softmax for columns 2c4 and 2c4+1 (the scores are
+    //      already scaled by scale * log2 e, folded into q~)
     float sc4[kStepTiles][4];
-    const bool need_mask = !(j0 >= u.lo_any && j0 + kStepKeys - 1 <= u.hi_any);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int t = 0; t < kStepTiles; ++t) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            float v = (s[t][0][e] + s[t][1][e]) * a.sl;
-            if (need_mask) {
+            float v = s[t][0][e] + s[t][1][e];
+            if constexpr (MASK) {
                 const int j = j0 + t * kTile + g8 + 8 * (e >> 1);
                 const bool ok = (e & 1) ? (j >= u.lo1 && j <= u.hi1) : (j >= u.lo0 && j <= u.hi0);
                 v = ok ? v : -INFINITY;
@@ -457,14 +460,15 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
         }
         u.m0 = mn0;
         u.m1 = mn1;
+        // the exponent reference: m, or 0 while a column has seen no key
+        u.mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        u.mu1 = mn1 == -INFINITY ? 0.f : mn1;
     }
-    const float mu0 = u.m0 == -INFINITY ? 0.f : u.m0;
-    const float mu1 = u.m1 == -INFINITY ? 0.f : u.m1;
     uint32_t bp[kStepTiles][2];
 #pragma unroll
     for (int t = 0; t < kStepTiles; ++t) {
-        const float p0 = ex2(sc4[t][0] - mu0), p1 = ex2(sc4[t][1] - mu1);
-        const float p2 = ex2(sc4[t][2] - mu0), p3 = ex2(sc4[t][3] - mu1);
+        const float p0 = ex2(sc4[t][0] - u.mu0), p1 = ex2(sc4[t][1] - u.mu1);
+        const float p2 = ex2(sc4[t][2] - u.mu0), p3 = ex2(sc4[t][3] - u.mu1);
         u.l0 += p0 + p2;
         u.l1 += p1 + p3;
         bp[t][0] = movmatrix_t(pack_h2(p0, p1));
@@ -636,7 +640,7 @@ decode_kernel(DecArgs a) {
                     for (int e = 0; e < E; ++e) f[e] = f[e] / sv[e];
                 }
 #pragma unroll
-                for (int e = 0; e < E; ++e) f[e] *= a.inv_sqrt_d;
+                for (int e = 0; e < E; ++e) f[e] *= a.qscale;
                 reg_fwht<E>(f, lane);
                 store_halves<E>(ws.qt[col] + lane * E, f);
                 if (lane == 0) {
@@ -676,6 +680,7 @@ decode_kernel(DecArgs a) {
         }
         if (!any_real) { us.lo_any = 1; us.hi_any = 0; }
         us.m0 = us.m1 = -INFINITY;
+        us.mu0 = us.mu1 = 0.f;
         us.l0 = us.l1 = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -690,6 +695,15 @@ decode_kernel(DecArgs a) {
         us.lo0 = max(us.lo0, j_first); us.hi0 = min(us.hi0, j_last - 1);
         us.lo1 = max(us.lo1, j_first); us.hi1 = min(us.hi1, j_last - 1);
         us.lo_all = max(us.lo_all, j_first); us.hi_all = min(us.hi_all, j_last - 1);
+        // a step in [lo_any, hi_any] needs no per-column bounds
+        auto step = [&](const SC &c, int jj) {
+            if (jj >= us.lo_any && jj + kStepKeys - 1 <= us.hi_any)
+                process_step<D, DK, DV, FAST, false>(c, jj, us, a, kbase, vbase, krow, vrow, g8,
+                                                     c4, smem_raw, klane, vlane);
+            else
+                process_step<D, DK, DV, FAST, true>(c, jj, us, a, kbase, vbase, krow, vrow, g8,
+                                                    c4, smem_raw, klane, vlane);
+        };
         SC ca, cb;
         int j = j_first;
         if (j < j_last) load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
@@ -699,14 +713,12 @@ decode_kernel(DecArgs a) {
             // once per two steps (j - j_first is a multiple of 64 here): the
             // next 64 keys, kPrefetchTiles tiles ahead
             prefetch(j + kPrefetchTiles * kTile, kPfKeys);
-            process_step<D, DK, DV, FAST>(ca, j, us, a, kbase, vbase, krow, vrow, g8, c4,
-                                          smem_raw, klane, vlane);
+            step(ca, j);
             j += kStepKeys;
             if (j >= j_last) break;
             if (j + kStepKeys < j_last)
                 load_step<D, DK, DV, FAST>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
-            process_step<D, DK, DV, FAST>(cb, j, us, a, kbase, vbase, krow, vrow, g8, c4,
-                                          smem_raw, klane, vlane);
+            step(cb, j);
             j += kStepKeys;
         }
 
@@ -1081,8 +1093,7 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.Nv = a.v_n_centroids;
     da.smooth = a.smooth;
     da.smooth_mode = a.smooth_mode;
-    da.sl = a.scale * kLog2e;
-    da.inv_sqrt_d = (float)(1.0 / sqrt((double)a.D));
+    da.qscale = (float)(1.0 / sqrt((double)a.D) * (double)a.scale * kLog2e);
     da.causal = a.causal;
     da.window = a.sliding_window;
     da.stride = a.kv_stride > 0 ? a.kv_stride : a.S_kv;
