@@ -50,10 +50,16 @@ constexpr float kSlack = 8.f;    // base-2 headroom of a column's reference maxi
 
 // ------------------------------------------------------------ primitives
 
+// The shared-memory gathers, products and transposes below are plain asm
+// (not volatile): they only read registers and the codebook tables, which
+// do not change after the block's set-up barrier, so the compiler may
+// schedule them freely (e.g. a tile's value gathers ahead of its softmax).
+// Global loads of codes stay volatile: they must not move above the
+// dependent-launch wait.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                          uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -62,7 +68,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n"
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n"
                  : "=r"(y) : "r"(x));
     return y;
 }
@@ -140,18 +146,18 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *w, int cb, int run0,
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    asm("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+    asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
 
@@ -184,12 +190,12 @@ __device__ __forceinline__ uint32_t row_off(uint32_t w, int i, uint32_t lane_off
 template <int SUB>
 __device__ __forceinline__ void gather_sh(uint32_t addr, uint32_t *w) {
     if constexpr (SUB == 2) {
-        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(w[0]) : "r"(addr));
+        asm("ld.shared.u32 %0, [%1];\n" : "=r"(w[0]) : "r"(addr));
     } else if constexpr (SUB == 4) {
-        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
+        asm("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
     } else {
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+        asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
     }
 }
 
@@ -338,6 +344,125 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t *p, uint32_t bytes) {
                      : "memory");
 }
 
+// ---- per-warp ring of code stages (uint8 code rows of 16-byte multiples)
+// Lane 0 of every warp streams the K and V code rows of its next steps into
+// a ring of stages in shared memory with bulk copies (cp.async.bulk, one per
+// operand and step, completing on the stage's mbarrier), kRingAhead steps
+// ahead of the warp; the lanes read a step's codes from its stage just
+// before the step.  Tile row r of a step holds key perm_row(r), which makes
+// both the key-code reads (lane rows g, g + 8) and the value-code reads
+// (lane rows 2c, 2c + 1, 2c + 8, 2c + 9) of 32-byte rows bank-conflict-free.
+template <int D, int DK, int DV>
+struct RingCfg {
+    static constexpr int KROW = D / DK, VROW = D / DV;   // code bytes per key
+    static constexpr bool on = KROW % 16 == 0 && VROW % 16 == 0;
+    static constexpr int STAGE = kStepKeys * (KROW + VROW);
+};
+constexpr uint32_t kRingAddr = 131072;        // shared address of the rings (after the table)
+constexpr uint32_t kSmemLimit = 232448;       // 227 KiB of dynamic shared memory per block
+constexpr uint32_t kRingPolls = 1u << 22;     // bound of every stage wait
+
+__host__ __device__ constexpr int ring_stages(int stage_bytes, int warps) {
+    return (int)((kSmemLimit - kRingAddr) / (uint32_t)(stage_bytes * warps)) > 4
+               ? 4
+               : (int)((kSmemLimit - kRingAddr) / (uint32_t)(stage_bytes * warps));
+}
+
+__device__ __forceinline__ int perm_row(int r) { return r ^ ((r >> 2) & 1); }
+
+__device__ __forceinline__ void ring_bar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void ring_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void ring_copy(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// bounded wait for phase `parity` of a stage's mbarrier: false if it expired
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kRingPolls; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+// NB bytes of shared memory at addr (after the stage's wait: volatile)
+template <int NB>
+__device__ __forceinline__ void lds_bytes(uint32_t addr, uint32_t *w) {
+    if constexpr (NB == 16) {
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr) : "memory");
+    } else if constexpr (NB == 8) {
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr) : "memory");
+    } else if constexpr (NB == 4) {
+        asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(w[0]) : "r"(addr) : "memory");
+    } else {
+        unsigned short v;
+        asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr) : "memory");
+        w[0] = v;
+    }
+}
+
+// A step's codes from its stage: K rows perm_row(g8) (+ 8) of each tile,
+// codes [c4 NKL, c4 NKL + NKL); V rows perm_row(vrow_of(c4, r)), codes
+// [g8 NVL, g8 NVL + NVL).
+template <int D, int DK, int DV>
+__device__ __forceinline__ void load_step_ring(StepCodes<D, DK, DV> &sc, uint32_t st, int g8,
+                                               int c4) {
+    using SC = StepCodes<D, DK, DV>;
+    using R = RingCfg<D, DK, DV>;
+    const int pk = perm_row(g8);
+#pragma unroll
+    for (int t = 0; t < kStepTiles; ++t) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            lds_bytes<SC::NKL>(st + (uint32_t)((t * kTile + pk + 8 * r) * R::KROW + c4 * SC::NKL),
+                               sc.k[t][r]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            lds_bytes<SC::NVL>(st + (uint32_t)(kStepKeys * R::KROW +
+                                               (t * kTile + perm_row(vrow_of(c4, r))) * R::VROW +
+                                               g8 * SC::NVL),
+                               sc.v[t][r]);
+    }
+}
+
+// The tiles of a warp's share that belong to one unit, and the keys its
+// steps cover: [j_first, j_last), clipped to the keys some query row of
+// batch b can see, [max(0, L - S_q - W + 1), L - 1] (no lower bound without
+// a window), so ragged caches read no codes past a batch's length.
+struct SegInfo {
+    int64_t unit, seg_end, bg;
+    int b, g, cblk, kv_len, j_first, j_last;
+};
+__device__ __forceinline__ SegInfo segment_at(const DecArgs &a, int64_t t, int64_t t_end) {
+    SegInfo sg;
+    sg.unit = t / a.T;
+    sg.seg_end = min(t_end, (sg.unit + 1) * (int64_t)a.T);
+    sg.cblk = (int)(sg.unit % a.n_colblk);
+    sg.bg = sg.unit / a.n_colblk;
+    sg.g = (int)(sg.bg % a.H_kv);
+    sg.b = (int)(sg.bg / a.H_kv);
+    // keys held by batch b (clamped to the cache)
+    sg.kv_len = a.kv_lens ? min(max(a.kv_lens[sg.b], 0), a.S_kv) : a.S_kv;
+    const int vis_lo = a.window > 0 ? max(0, sg.kv_len - a.S_q - a.window + 1) : 0;
+    const int vis_end = (sg.kv_len + kTile - 1) / kTile * kTile;
+    sg.j_first = max((int)((a.tlo + (t - sg.unit * (int64_t)a.T)) * kTile), vis_lo / kTile * kTile);
+    sg.j_last = min((int)((a.tlo + (sg.seg_end - sg.unit * (int64_t)a.T)) * kTile),
+                    vis_end);  // exclusive
+    return sg;
+}
+
 // Per-warp state of one unit (batch, kv head, column block).
 template <int D>
 struct UnitState {
@@ -367,7 +492,7 @@ __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const 
 // One 32-key step.  MASK: the step needs the per-column key bounds (the
 // first and last steps of a segment); the steps between take the unmasked
 // instantiation, in which every real column sees every key.
-template <int D, int DK, int DV, bool FAST, bool MASK>
+template <int D, int DK, int DV, bool FAST, bool MASK, bool PERM>
 __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int j0,
                                              UnitState<D> &u, const DecArgs &a,
                                              uint32_t kbase, uint32_t vbase, int krow,
@@ -429,7 +554,9 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
         for (int e = 0; e < 4; ++e) {
             float v = s[t][0][e] + s[t][1][e];
             if constexpr (MASK) {
-                const int j = j0 + t * kTile + g8 + 8 * (e >> 1);
+                // S row g8 (+ 8) of tile t holds key perm_row(g8) (+ 8) of
+                // a ring stage, key g8 (+ 8) otherwise
+                const int j = j0 + t * kTile + (PERM ? perm_row(g8) : g8) + 8 * (e >> 1);
                 const bool ok = (e & 1) ? (j >= u.lo1 && j <= u.hi1) : (j >= u.lo0 && j <= u.hi0);
                 v = ok ? v : -INFINITY;
             }
@@ -519,7 +646,14 @@ decode_kernel(DecArgs a) {
     unsigned char *vtab = FAST ? ktab + 128 : smem_raw + align16((size_t)a.Nk * krow);
     WarpScratch<D> *scratch = reinterpret_cast<WarpScratch<D> *>(smem_raw + tab_bytes);
     float *stage = reinterpret_cast<float *>(scratch + kWarps);
-    if (FAST && (uint32_t)__cvta_generic_to_shared(stage + a.Nk * DK + a.Nv * DV) > kFastTabAddr)
+    // ring path (uint8 codes in rows of 16-byte multiples): the stage
+    // mbarriers after the staging area, the stages from shared address 128 KiB
+    using RC = RingCfg<D, DK, DV>;
+    constexpr bool RING = FAST && RC::on;
+    constexpr int kStages = RING ? ring_stages(RC::STAGE, kWarps) : 1;
+    const uint32_t mbar0 =
+        ((uint32_t)__cvta_generic_to_shared(stage + a.Nk * DK + a.Nv * DV) + 7u) & ~7u;
+    if (FAST && mbar0 + (RING ? kWarps * kStages * 8 : 0) > kFastTabAddr)
         return;   // not reachable: dynamic shared memory starts near address 0
     const int kstride = FAST ? (int)kFastRow : krow;   // row strides of the tables
     const int vstride = FAST ? (int)kFastRow : vrow;
@@ -583,32 +717,72 @@ decode_kernel(DecArgs a) {
     int64_t t = share_start(gw, a.share, a.total);
     const int64_t t_end = share_start(gw + 1, a.share, a.total);
     int slot = 0;
+
+    // ---- ring path: the producer cursor walks the warp's steps ahead of it
+    const uint32_t wbar = mbar0 + (uint32_t)(warp * kStages * 8);
+    const uint32_t wring = kRingAddr + (uint32_t)(warp * kStages * RC::STAGE);
+    SegInfo ps{};
+    int64_t pt = t;
+    int pj = 0, issued = 0;
+    bool pvalid = false, ring_ok = true;
+    uint32_t pending = 0u, pend_par = 0u;   // stages with a copy in flight, and its phase
+    auto pseek = [&]() {   // to the next step of a non-empty segment
+        while (pj >= ps.j_last) {
+            pt = ps.seg_end;
+            if (pt >= t_end) { pvalid = false; return; }
+            ps = segment_at(a, pt, t_end);
+            pj = ps.j_first;
+        }
+    };
+    // copy the next step's K and V code rows into stage issued % kStages
+    auto issue = [&]() {
+        if (!pvalid) return;
+        const int sidx = issued % kStages;
+        const uint32_t bar = wbar + (uint32_t)(sidx * 8);
+        const uint32_t st = wring + (uint32_t)(sidx * RC::STAGE);
+        const int n = min(kStepKeys, a.S_kv - pj);   // rows inside the cache
+        if (lane == 0) {
+            // the stage was last read by this warp's lanes (generic proxy)
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            ring_expect(bar, (uint32_t)(n * (RC::KROW + RC::VROW)));
+            ring_copy(st, a.kc + (ps.bg * a.stride + pj) * RC::KROW, (uint32_t)(n * RC::KROW), bar);
+            ring_copy(st + kStepKeys * RC::KROW, a.vc + (ps.bg * a.stride + pj) * RC::VROW,
+                      (uint32_t)(n * RC::VROW), bar);
+        }
+        pending |= 1u << sidx;
+        pend_par = (pend_par & ~(1u << sidx)) | ((uint32_t)((issued / kStages) & 1) << sidx);
+        ++issued;
+        pj += kStepKeys;
+        pseek();
+    };
+    if constexpr (RING) {
+        if (lane == 0) {
+            for (int k = 0; k < kStages; ++k) ring_bar_init(wbar + (uint32_t)(k * 8));
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        }
+        __syncwarp();
+        if (t < t_end) {
+            ps = segment_at(a, t, t_end);
+            pj = ps.j_first;
+            pvalid = true;
+            pseek();
+        }
+        for (int k = 0; k < kStages; ++k) issue();
+    }
+    int consumed = 0;
+
     while (t < t_end) {
-        const int64_t unit = t / a.T;
-        const int64_t seg_end = min(t_end, (unit + 1) * (int64_t)a.T);
-        const int cblk = (int)(unit % a.n_colblk);
-        const int64_t bg = unit / a.n_colblk;
-        const int g = (int)(bg % a.H_kv);
-        const int b = (int)(bg / a.H_kv);
+        const SegInfo sg = segment_at(a, t, t_end);
+        const int64_t unit = sg.unit, seg_end = sg.seg_end, bg = sg.bg;
+        const int cblk = sg.cblk, g = sg.g, b = sg.b, kv_len = sg.kv_len;
+        const int j_first = sg.j_first, j_last = sg.j_last;
         // the segment's first code tiles go to L2 while the queries are prepared
         const uint8_t *kg = a.kc + bg * a.stride * ktb;
         const uint8_t *vg = a.vc + bg * a.stride * vtb;
-        // keys held by batch b (clamped to the cache)
-        const int kv_len = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
         // lane base pointers: row g8 of a tile (K), row 2c4 of a tile (V)
         // (packed rows: the row start; the run's first code index is passed on)
         const uint8_t *kl = kg + (int64_t)g8 * ktb + (a.kcb > 0 ? (int64_t)c4 * SC::NKL * a.kcb : 0);
         const uint8_t *vl = vg + (int64_t)(2 * c4) * vtb + (a.vcb > 0 ? (int64_t)g8 * SC::NVL * a.vcb : 0);
-        // the segment covers tiles [t, seg_end) of the unit; steps are 2 tiles
-        // clipped to the keys some query row of batch b can see,
-        // [max(0, L - S_q - W + 1), L - 1] (no lower bound without a window),
-        // so ragged caches read no codes past a batch's length
-        const int vis_lo = a.window > 0 ? max(0, kv_len - a.S_q - a.window + 1) : 0;
-        const int vis_end = (kv_len + kTile - 1) / kTile * kTile;
-        const int j_first = max((int)((a.tlo + (t - unit * (int64_t)a.T)) * kTile),
-                                vis_lo / kTile * kTile);
-        const int j_last = min((int)((a.tlo + (seg_end - unit * (int64_t)a.T)) * kTile),
-                               vis_end);  // exclusive
         // L2 prefetch of the keys [j, j + n) (clipped to the segment and the cache)
         auto prefetch = [&](int j, int n) {
             const int e = min(min(j + n, j_last), a.S_kv);
@@ -617,7 +791,7 @@ decode_kernel(DecArgs a) {
                 prefetch_l2(vg + (int64_t)j * vtb, (uint32_t)((e - j) * vtb));
             }
         };
-        prefetch(j_first, kPrefetchTiles * kTile);
+        if constexpr (!RING) prefetch(j_first, kPrefetchTiles * kTile);
 
         // ---- transformed queries of the unit's columns: q~ = Hn (q (.) s_g^-1)
         __syncwarp();
@@ -698,12 +872,31 @@ decode_kernel(DecArgs a) {
         // a step in [lo_any, hi_any] needs no per-column bounds
         auto step = [&](const SC &c, int jj) {
             if (jj >= us.lo_any && jj + kStepKeys - 1 <= us.hi_any)
-                process_step<D, DK, DV, FAST, false>(c, jj, us, a, kbase, vbase, krow, vrow, g8,
-                                                     c4, smem_raw, klane, vlane);
+                process_step<D, DK, DV, FAST, false, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
+                                                           g8, c4, smem_raw, klane, vlane);
             else
-                process_step<D, DK, DV, FAST, true>(c, jj, us, a, kbase, vbase, krow, vrow, g8,
-                                                    c4, smem_raw, klane, vlane);
+                process_step<D, DK, DV, FAST, true, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
+                                                          g8, c4, smem_raw, klane, vlane);
         };
+        if constexpr (RING) {
+            // steps from the ring: wait for the stage, read its codes, hand
+            // it back to the producer (which refills it kStages steps ahead)
+            for (int j = j_first; j < j_last; j += kStepKeys) {
+                const int sidx = consumed % kStages;
+                const uint32_t bar = wbar + (uint32_t)(sidx * 8);
+                if (ring_ok) {
+                    const bool ok = ring_wait(bar, (uint32_t)((consumed / kStages) & 1));
+                    ring_ok = __all_sync(0xffffffffu, ok);
+                    if (ring_ok) pending &= ~(1u << sidx);
+                }
+                SC sc;
+                load_step_ring<D, DK, DV>(sc, wring + (uint32_t)(sidx * RC::STAGE), g8, c4);
+                __syncwarp();
+                ++consumed;
+                if (ring_ok) issue();
+                step(sc, j);
+            }
+        } else {
         SC ca, cb;
         int j = j_first;
         if (j < j_last) load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
@@ -721,8 +914,11 @@ decode_kernel(DecArgs a) {
             step(cb, j);
             j += kStepKeys;
         }
+        }
 
         // ---- this warp's partial record for the unit
+        // (a stage wait that expired leaves the record, hence the output, NaN)
+        if (RING && !ring_ok) us.l0 = us.l1 = NAN;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             us.l0 += __shfl_xor_sync(0xffffffffu, us.l0, off);
@@ -747,6 +943,13 @@ decode_kernel(DecArgs a) {
         }
         ++slot;
         t = seg_end;
+    }
+    // a stage wait expired: wait (bounded) for this warp's copies still in flight
+    if constexpr (RING) {
+        if (!ring_ok) {
+            for (int k = 0; k < kStages; ++k)
+                if (pending & (1u << k)) ring_wait(wbar + (uint32_t)(k * 8), (pend_par >> k) & 1u);
+        }
     }
 }
 
@@ -914,11 +1117,20 @@ Tables choose_tables(const vq_attend_args &a) {
     const size_t tail = scratch_bytes(a.D) +
                         sizeof(float) * ((size_t)a.k_n_centroids * a.k_sub_dim +
                                          (size_t)a.v_n_centroids * a.v_sub_dim);
-    // fast path: the table sits at shared address 64 KiB, scratch and
-    // staging below it (dynamic shared memory starts within the first KiB)
+    // fast path: the table sits at shared address 64 KiB, scratch, staging
+    // and the ring mbarriers below it (dynamic shared memory starts within
+    // the first KiB); code rows of 16-byte multiples also take the per-warp
+    // rings of code stages from 128 KiB on
+    const int krowb = a.D / a.k_sub_dim, vrowb = a.D / a.v_sub_dim;
+    const bool ring = krowb % 16 == 0 && vrowb % 16 == 0;
+    const int stage = kStepKeys * (krowb + vrowb);
+    const int warps = warps_for(a.D);
+    const size_t mbars = ring ? (size_t)warps * ring_stages(stage, warps) * 8 + 8 : 0;
     if (a.k_code_bytes == 1 && a.v_code_bytes == 1 && a.k_n_centroids <= 256 &&
-        a.v_n_centroids <= 256 && tail + 2048 <= kFastTabAddr)
-        return {128 / ek, 128 / ev, true, 2 * (size_t)kFastTabAddr};
+        a.v_n_centroids <= 256 && tail + mbars + 2048 <= kFastTabAddr)
+        return {128 / ek, 128 / ev, true,
+                ring ? (size_t)kRingAddr + (size_t)warps * ring_stages(stage, warps) * stage
+                     : 2 * (size_t)kFastTabAddr};
     int kc = 128 / ek, vc = 128 / ev;
     auto total = [&](int k, int v) {
         return align16((size_t)a.k_n_centroids * k * ek) +
@@ -1008,7 +1220,7 @@ int decode_supported(const vq_attend_args &a) {
     if (a.D != 32 && a.D != 64 && a.D != 128 && a.D != 256) return VQ_ERR_UNSUPPORTED;
     if (!pair_ok(a.D, a.k_sub_dim, a.v_sub_dim)) return VQ_ERR_UNSUPPORTED;
     const Tables tb = choose_tables(a);
-    if (tb.bytes > kSmemBudget) return VQ_ERR_UNSUPPORTED;
+    if (tb.bytes > (tb.fast ? (size_t)kSmemLimit : kSmemBudget)) return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
 }
 
