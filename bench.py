@@ -53,8 +53,8 @@ METRICS = {
     "bulk-encode-packed": ("key-encode vectors/s ([4,32,8192,128] K+V encode, 10-bit packed "
                            "key codes, 20 B/token-head)", "vectors/s"),
     "chunked-prefill": ("prefill tokens/s (S_q=2048, window 4096)", "tokens/s"),
-    "decode-append": ("decode tokens/s (append 1 token's K/V codes into a 8256-row cache + "
-                      "attend over 8192, B=1 H=8 D=128)", "tokens/s"),
+    "decode-append": ("decode tokens/s (one launch: append 1 token's K/V codes into a 8256-row "
+                      "cache + attend over 8192, B=1 H=8 D=128)", "tokens/s"),
     "gqa-decode-ragged": ("decode tokens/s (B=32 Hq=32 Hkv=8, cache lengths U[16384, 32768])",
                           "tokens/s"),
 }
@@ -274,17 +274,14 @@ class Runner:
                              s.window, out=d["out"], workspace=d["ws"], stream=st)
             return 3
         if self.name == "decode-append":
-            vq.encode_keys_into(d["keys"], d["k_codebook"], s.k_d, d["smooth"],
-                                d["k_codes"], s.S_kv - 1, stream=st)
-            vq.encode_values_into(d["values"], d["v_codebook"], s.v_d, d["v_codes"],
-                                  s.S_kv - 1, stream=st)
+            # one launch: the new token's K and V into row S_kv - 1, attention
+            # over the S_kv cached tokens, merge of the key splits
             if ev: ev[0].record(st)
-            vq.decode_attend(d["q"], d["k_codes"], d["k_codebook"], d["v_codes"],
-                             d["v_codebook"], d["smooth"], s.sm_scale, s.causal,
-                             s.window, out=d["out"], workspace=d["ws"], stream=st,
-                             s_kv=s.S_kv)
+            vq.decode_step(d["q"], d["keys"], d["values"], d["k_codes"], d["k_codebook"],
+                           d["v_codes"], d["v_codebook"], d["smooth"], s.sm_scale, s.causal,
+                           s.window, out=d["out"], workspace=d["ws"], stream=st, s_kv=s.S_kv)
             if ev: ev[1].record(st)
-            return 4
+            return 1
         if self.name.startswith("bulk-encode"):
             if ev: ev[0].record(st)
             vq.encode_keys(d["keys"], d["k_codebook"], s.k_d, d["smooth"],

@@ -247,6 +247,34 @@ VQ_API size_t vq_attend_workspace_bytes(const vq_attend_args *args);
 VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
 
 /*
+ * One decode step of the cache in one launch.  Page "veloxquant_mlx.cache.
+ * vecinfer_cache module", VecInferKVCache.update_and_fetch (the new tokens
+ * are encoded and stored after the cached ones) followed by its fused_sdpa
+ * over the updated cache.
+ *
+ *   k_new_f16, v_new_f16  [B, H_kv, S_q, D] fp16: the keys and values of the
+ *              S_q new tokens (the tokens of the queries).
+ *   args       as for vq_decode_attend, with S_kv counting the new tokens:
+ *              their codes are written into rows S_kv - S_q .. S_kv - 1 of
+ *              every (b, kv head) of k_codes / v_codes (the other rows are
+ *              not touched), encoded exactly as vq_encode_keys_into (with
+ *              k_codebook, smooth) and vq_encode_values_into (v_codebook)
+ *              would; then every query attends over rows 0 .. S_kv - 1 as
+ *              in vq_decode_attend.  kv_lens must be NULL.
+ * With D = 128, 4-dimensional sub-vectors, uint8 codes and codebooks of at
+ * most 256 centroids this is one cooperative launch (encode, grid sync,
+ * attention, grid sync, merge of the key splits); other shapes run as the
+ * three calls on the same stream.  The workspace is as for
+ * vq_decode_attend.
+ * Errors: those of vq_decode_attend and of the encodes; VQ_ERR_SHAPE when
+ * S_q > S_kv, VQ_ERR_UNSUPPORTED when kv_lens is given, VQ_ERR_NULL /
+ * VQ_ERR_ALIGN for the new tokens, VQ_ERR_CUDA when the launch fails (e.g.
+ * the grid cannot be resident at once).
+ */
+VQ_API int vq_decode_step(const vq_attend_args *args, const void *k_new_f16,
+                          const void *v_new_f16, void *stream);
+
+/*
  * Same operation through the tcgen05 tensor-core path (key/value tiles
  * rebuilt from codes in shared memory, Q~K~^T and PV on the tensor cores,
  * accumulators in tensor memory).  Used when S_q >= 64; smaller S_q, or

@@ -29,7 +29,7 @@ VQ_ERR_CUDA = -6
 EXPORTED = ("vq_status_str", "vq_encode_keys", "vq_encode_values",
             "vq_encode_keys_into", "vq_encode_values_into",
             "vq_dequant", "vq_attend_workspace_bytes", "vq_decode_attend",
-            "vq_prefill_attend", "vq_decode_attend_noalloc")
+            "vq_prefill_attend", "vq_decode_attend_noalloc", "vq_decode_step")
 
 
 class VQError(RuntimeError):
@@ -94,10 +94,11 @@ def lib():
         L.vq_decode_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
         L.vq_prefill_attend.argtypes = [ctypes.POINTER(AttendArgs), vp]
         L.vq_decode_attend_noalloc.argtypes = [ctypes.POINTER(AttendArgs), vp]
+        L.vq_decode_step.argtypes = [ctypes.POINTER(AttendArgs), vp, vp, vp]
         for fn in ("vq_encode_keys", "vq_encode_values", "vq_encode_keys_into",
                    "vq_encode_values_into", "vq_dequant",
                    "vq_decode_attend", "vq_prefill_attend",
-                   "vq_decode_attend_noalloc"):
+                   "vq_decode_attend_noalloc", "vq_decode_step"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -318,6 +319,33 @@ def decode_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,
     return _attend("vq_decode_attend", q, k_codes, k_codebook, v_codes,
                    v_codebook, smooth, scale, causal, sliding_window, out,
                    workspace, stream, s_kv, kv_lens)
+
+
+def decode_step(q, k_new, v_new, k_codes, k_codebook, v_codes, v_codebook, smooth,
+                scale=None, causal=True, sliding_window=0, out=None, workspace=None,
+                stream=None, s_kv=None) -> torch.Tensor:
+    """vq_decode_step: encode k_new / v_new [B, H_kv, S_q, D] into rows
+    s_kv - S_q .. s_kv - 1 of the code buffers, then attend (one launch)."""
+    D = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    for t in (k_new, v_new):
+        if t.dtype != torch.float16 or not t.is_contiguous():
+            raise VQError(VQ_ERR_SHAPE, "k_new / v_new must be contiguous fp16")
+    a = make_attend_args(q, k_codes, k_codebook, v_codes, v_codebook, smooth, scale, causal,
+                         sliding_window, out, workspace, s_kv, None)
+    if workspace is None:
+        need = attend_workspace_bytes(a)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            a.workspace = workspace.data_ptr()
+            a.workspace_bytes = need
+    st = lib().vq_decode_step(ctypes.byref(a), k_new.data_ptr(), v_new.data_ptr(),
+                              _stream(stream))
+    _check(st, "vq_decode_step")
+    return out
 
 
 def prefill_attend(q, k_codes, k_codebook, v_codes, v_codebook, smooth,

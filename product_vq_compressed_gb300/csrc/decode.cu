@@ -31,6 +31,7 @@
 //   * Each CTA merges its warps and writes one partial (m, l, o[D]) per
 //     column; the combine kernel merges the splits and writes fp16.
 #include <climits>
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "vq_internal.cuh"
@@ -250,7 +251,34 @@ struct DecArgs {
     int nw;            // warps sharing the work
     int slots;         // partial records per warp
     int k_copies, v_copies;
+    // one decode step in one cooperative launch (vq_decode_step): encode the
+    // new tokens into cache rows new_row0 .., grid sync, attend, grid sync,
+    // merge the key splits
+    int step;
+    const __half *k_new, *v_new;   // [B, H_kv, S_q, D]
+    int new_row0;
+    int log2D;
+    __half *out;
 };
+
+// Record of warp w for unit `unit`, column col: the warps whose shares
+// overlap the unit's tiles [unit T, unit T + T) each hold one, in the slot
+// of that unit among the units their share touches.
+__device__ __forceinline__ float *unit_record(const DecArgs &a, int64_t unit, int64_t w, int col,
+                                              int D) {
+    const int64_t u0 = unit * a.T;
+    const int64_t s = w * a.share;
+    const int64_t slot = a.share <= a.T ? (s >= u0 ? 0 : 1) : unit - s / a.T;
+    return a.ws + ((w * a.slots + slot) * kCols + col) * (int64_t)(D + 4);
+}
+__device__ __forceinline__ void unit_warps(const DecArgs &a, int64_t unit, int64_t *w_lo,
+                                           int *n_rec) {
+    const int64_t u0 = unit * a.T;
+    *w_lo = u0 / a.share;
+    int64_t w_hi = (u0 + a.T - 1) / a.share;
+    if (w_hi > a.nw - 1) w_hi = a.nw - 1;
+    *n_rec = (int)(w_hi - *w_lo + 1);
+}
 
 // Warp gw's contiguous share of the flattened (unit, tile) space is
 // [gw * share, min((gw + 1) * share, total)).
@@ -624,6 +652,131 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
     }
 }
 
+// Encode of one new token by one warp, D = 32 E with sub-vectors of E
+// dimensions (lane m owns sub-vector m), into its 32-byte uint8 code row
+// (cb: the fp32 codebook, staged in shared memory by the caller):
+// the same definition and decision rule as the encode kernels -- smooth and
+// Walsh-Hadamard rotation (keys), nearest centroid by the direct-form fp32
+// distance to every centroid, lowest index on ties, kept when the rounding
+// certificate holds and decided again in float-float otherwise.
+template <int E>
+__device__ void encode_token_warp(const __half *x, const float *sm, int rotate, const float *cb,
+                                  int N, uint8_t *dst, int log2D, int lane) {
+    const float inv_sqrt_d = 1.f / sqrtf((float)(32 * E));
+    float f[E];
+    load_halves<E>(x + lane * E, f);
+    float asum = 0.f;
+    if (rotate) {
+        if (sm) {
+            float sv[E];
+            load_floats<E>(sm + lane * E, sv);
+#pragma unroll
+            for (int j = 0; j < E; ++j) f[j] *= sv[j];
+        }
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            asum += fabsf(f[j]);
+            f[j] *= inv_sqrt_d;
+        }
+        reg_fwht<E>(f, lane);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, off);
+    const float delta = rotate ? asum * rotation_delta_coef(log2D, inv_sqrt_d) : 0.f;
+    float b = INFINITY, b2 = INFINITY;
+    int bi = 0;
+#pragma unroll 8
+    for (int c = 0; c < N; ++c) {
+        float cv[E];
+        load_floats<E>(cb + (size_t)c * E, cv);
+        float d = 0.f;
+#pragma unroll
+        for (int t = 0; t < E; ++t) {
+            const float e = f[t] - cv[t];
+            d = fmaf(e, e, d);
+        }
+        b2 = fminf(b2, fmaxf(b, d));
+        if (d < b) { b = d; bi = c; }
+    }
+    int code = bi;
+    unsigned m = __ballot_sync(0xffffffffu, !code_certified<E>(b, b2, delta));
+    while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int cx = nearest_exact_e<E, E>(
+            x, sm, rotate, [cb](int c, int t) { return cb[(size_t)c * E + t]; }, N, src,
+            __shfl_sync(0xffffffffu, delta, src), lane);
+        if (lane == src) code = cx;
+    }
+    dst[lane] = (uint8_t)code;
+}
+
+// Merge of the key splits inside a decode step (after the grid sync): CTA
+// c takes the (unit, column, 32 output dimensions) items c, c + grid, ...;
+// its warps split the item's records, each lane one output dimension; the
+// maxima, sums and partial outputs are reduced in shared memory (`sm` >=
+// (32 kWarps + 2 kWarps) floats), out = o / l in fp16.
+template <int D, int kWarps>
+__device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
+    float *part = sm;                      // [kWarps][32]
+    float *red = sm + kWarps * 32;         // [2][kWarps]
+    const int64_t units = a.total / a.T;
+    const int ncb = min(kCols, a.G * a.S_q);
+    constexpr int nch = D / 32;
+    const int64_t items = units * ncb * nch;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int ch = (int)(it % nch);
+        const int64_t unit = it / nch / ncb;
+        const int col = (int)(it / nch % ncb);
+        const int cblk = (int)(unit % a.n_colblk);
+        if (cblk * kCols + col >= a.G * a.S_q) continue;   // block-uniform
+        int64_t w_lo;
+        int n_rec;
+        unit_warps(a, unit, &w_lo, &n_rec);
+        // maximum over the records
+        float M = -INFINITY;
+        for (int k = warp * 32 + lane; k < n_rec; k += kWarps * 32)
+            M = fmaxf(M, __ldcg(unit_record(a, unit, w_lo + k, col, D)));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (lane == 0) red[warp] = M;
+        __syncthreads();
+        M = red[0];
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
+        // each warp: its records' weighted sums (every record of a warp
+        // loaded before any is used)
+        float l = 0.f, o = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll 4
+            for (int k = warp; k < n_rec; k += kWarps) {
+                const float *r = unit_record(a, unit, w_lo + k, col, D);
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(r));
+                const float ov = __ldcg(r + 4 + ch * 32 + lane);
+                const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+                l = fmaf(f, ml.y, l);
+                o = fmaf(f, ov, o);
+            }
+        }
+        part[warp * 32 + lane] = o;
+        if (lane == 0) red[kWarps + warp] = l;
+        __syncthreads();
+        if (warp == 0) {
+            float lt = 0.f, acc = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                lt += red[kWarps + w];
+                acc += part[w * 32 + lane];
+            }
+            const int bgi = (int)(unit / a.n_colblk);
+            const int b = bgi / a.H_kv, g = bgi % a.H_kv;
+            const int cg = cblk * kCols + col;
+            const int i = cg / a.G, hq = g * a.G + cg % a.G;
+            a.out[(((int64_t)b * a.H_q + hq) * a.S_q + i) * D + ch * 32 + lane] =
+                __float2half_rn(lt > 0.f ? acc / lt : 0.f);
+        }
+        __syncthreads();   // part[] and red[] are reused by the next item
+    }
+}
+
 template <int D, int DK, int DV, bool FAST>
 __global__ void __launch_bounds__(warps_for(D) * 32, 1)
 decode_kernel(DecArgs a) {
@@ -666,6 +819,12 @@ decode_kernel(DecArgs a) {
 
     // ---- fp16 tables replicated per bank group (rows past N are zero)
     if constexpr (FAST) {
+        // a decode step's encode reads the fp32 codebooks from the staging area
+        if (a.step) {
+            const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
+            for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
+            for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
+        }
         // 256 rows x 16 chunks of 16 bytes (8 key, 8 value); every chunk of a
         // row half holds 16 / EK (16 / EV) copies of its centroid.  A thread
         // owns whole rows: both centroid loads are in flight together, then
@@ -712,10 +871,39 @@ decode_kernel(DecArgs a) {
     const int n_cols_total = a.G * a.S_q;
     WarpScratch<D> &ws = scratch[warp];
 
+    // ---- decode step: the new tokens' codes into the cache, then a grid sync
+    //      (every warp of the grid takes tokens; the attention below reads
+    //      them through the bulk copies, which need the proxy fence)
+    if constexpr (FAST && D == 128 && DK == 4 && DV == 4) {
+        if (a.step) {
+            const int n_new = a.B * a.H_kv * a.S_q;
+            const int gwarps = (int)gridDim.x * kWarps;
+            // tasks go to the CTAs first (task t: CTA t mod grid), so that a
+            // few tokens are encoded on as many SMs
+            for (int task = warp * (int)gridDim.x + (int)blockIdx.x; task < 2 * n_new;
+                 task += gwarps) {
+                const int tok = task >> 1, is_v = task & 1;
+                const int bh = tok / a.S_q, tt = tok - bh * a.S_q;
+                const int h = bh % a.H_kv;
+                const __half *x = (is_v ? a.v_new : a.k_new) + (int64_t)tok * D;
+                uint8_t *dst = const_cast<uint8_t *>(is_v ? a.vc : a.kc) +
+                               ((int64_t)bh * a.stride + a.new_row0 + tt) * 32;
+                const float *smr = is_v || a.smooth_mode == 0 ? nullptr
+                                   : a.smooth_mode == 2 ? a.smooth + (size_t)h * D : a.smooth;
+                encode_token_warp<4>(x, smr, !is_v, is_v ? stage + a.Nk * DK : stage,
+                                     is_v ? a.Nv : a.Nk, dst, a.log2D, lane);
+            }
+            __threadfence();
+            cooperative_groups::this_grid().sync();
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        }
+    }
+
+    // warps past the plan's last one have no share (they still reach the
+    // grid syncs of a decode step)
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
-    if (gw >= a.nw) return;
-    int64_t t = share_start(gw, a.share, a.total);
-    const int64_t t_end = share_start(gw + 1, a.share, a.total);
+    int64_t t = gw < a.nw ? share_start(gw, a.share, a.total) : 0;
+    const int64_t t_end = gw < a.nw ? share_start(gw + 1, a.share, a.total) : 0;
     int slot = 0;
 
     // ---- ring path: the producer cursor walks the warp's steps ahead of it
@@ -951,6 +1139,15 @@ decode_kernel(DecArgs a) {
                 if (pending & (1u << k)) ring_wait(wbar + (uint32_t)(k * 8), (pend_par >> k) & 1u);
         }
     }
+    // ---- decode step: every record written, then the merge of the splits
+    //      (the codebook table region is free now)
+    if constexpr (FAST && D == 128 && DK == 4 && DV == 4) {
+        if (a.step) {
+            __threadfence();
+            cooperative_groups::this_grid().sync();
+            merge_items<D, kWarps>(a, reinterpret_cast<float *>(ktab), warp, lane);
+        }
+    }
 }
 
 // Merge the partial records of every (unit, column) and write fp16.  The
@@ -1153,6 +1350,22 @@ cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tb.bytes);
     if (err != cudaSuccess) return err;
+    if (da.step) {
+        // a decode step: cooperative launch (its blocks meet at grid syncs;
+        // the launch fails rather than starting if they cannot all be
+        // resident at once)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(warps_for(D) * 32);
+        cfg.dynamicSmemBytes = tb.bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, da);
+    }
     return launch_dependent(kern, dim3(grid), dim3(warps_for(D) * 32), tb.bytes, stream, da);
 }
 
@@ -1226,6 +1439,17 @@ int decode_supported(const vq_attend_args &a) {
 
 size_t decode_smem_bytes(const vq_attend_args &a) { return choose_tables(a).bytes; }
 
+// The single-launch decode step: uint8 codes of 4-dimensional sub-vectors at
+// D = 128 (the shared-memory table and code-ring path), one grid of at most
+// one block per SM (the persistent plan), no per-batch lengths.
+int decode_step_supported(const vq_attend_args &a) {
+    if (a.D != 128 || a.k_sub_dim != 4 || a.v_sub_dim != 4) return VQ_ERR_UNSUPPORTED;
+    if (a.k_code_bytes != 1 || a.v_code_bytes != 1) return VQ_ERR_UNSUPPORTED;
+    if (a.kv_lens) return VQ_ERR_UNSUPPORTED;
+    if (!choose_tables(a).fast) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
+}
+
 // Work split: the (unit, key tile) space, units = (b, kv head, column
 // block), is cut into equal contiguous shares, one per warp of a persistent
 // grid of one CTA per SM (fewer when the problem is small).
@@ -1285,7 +1509,7 @@ AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms, size_t max_w
 }
 
 cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const void *k_new, const void *v_new) {
     const Tables tb = choose_tables(a);
     DecArgs da{};
     da.B = a.B; da.H_q = a.H_q; da.H_kv = a.H_kv; da.S_q = a.S_q; da.S_kv = a.S_kv;
@@ -1320,6 +1544,14 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.slots = plan.slots;
     da.k_copies = tb.k_copies;
     da.v_copies = tb.v_copies;
+    da.step = k_new != nullptr;
+    da.k_new = reinterpret_cast<const __half *>(k_new);
+    da.v_new = reinterpret_cast<const __half *>(v_new);
+    da.new_row0 = a.S_kv - a.S_q;
+    int l2d = 0;
+    while ((1 << l2d) < a.D) ++l2d;
+    da.log2D = l2d;
+    da.out = reinterpret_cast<__half *>(a.out_f16);
     cudaError_t err;
     switch (a.D) {
         case 32: err = launch_d<32>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
@@ -1328,7 +1560,7 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
         case 256: err = launch_d<256>(da, a.k_sub_dim, a.v_sub_dim, tb, plan.grid, stream); break;
         default: return cudaErrorInvalidValue;
     }
-    if (err != cudaSuccess) return err;
+    if (err != cudaSuccess || da.step) return err;   // a step merges in its own launch
     const int64_t units = plan.total / plan.tiles;
     const int cols = min(kCols, da.G * da.S_q);   // real columns of a column block
     __half *out = reinterpret_cast<__half *>(a.out_f16);

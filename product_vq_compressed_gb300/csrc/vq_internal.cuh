@@ -481,8 +481,13 @@ AttendPlan plan_decode(const vq_attend_args &a, int num_sms);
 // splits); n_split == 0 when even one split does not fit.
 AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,
                               size_t max_ws_bytes);
+// k_new / v_new (both or neither): one decode step in one cooperative
+// launch -- the new tokens [B, H_kv, S_q, D] are encoded into cache rows
+// S_kv - S_q .. S_kv - 1 first, and the key splits are merged in the launch.
 cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const void *k_new = nullptr,
+                          const void *v_new = nullptr);
+int decode_step_supported(const vq_attend_args &a);   // VQ_OK or a status
 size_t decode_smem_bytes(const vq_attend_args &a);
 int decode_supported(const vq_attend_args &a);   // VQ_OK or a status
 // The same arguments with packed rows of 8- or 16-bit codes described as

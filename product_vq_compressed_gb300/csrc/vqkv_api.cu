@@ -234,6 +234,41 @@ int vq_decode_attend(const vq_attend_args *args, void *stream) {
     return decode_impl(&n, stream);
 }
 
+int vq_decode_step(const vq_attend_args *in, const void *k_new_f16, const void *v_new_f16,
+                   void *stream) {
+    if (!in) return VQ_ERR_NULL;
+    const vq_attend_args n = vqkv::normalize_code_widths(*in);
+    const vq_attend_args *a = &n;
+    int rc = vqkv::attend_validate(a);
+    if (rc != VQ_OK) return rc;
+    if (a->S_q > a->S_kv) return VQ_ERR_SHAPE;   // the new tokens are cache rows
+    if (a->kv_lens) return VQ_ERR_UNSUPPORTED;   // one append offset for every batch
+    if ((int64_t)a->B * a->H_q * a->S_q == 0) return VQ_OK;
+    if (!k_new_f16 || !v_new_f16) return VQ_ERR_NULL;
+    if (!aligned16(k_new_f16) || !aligned16(v_new_f16)) return VQ_ERR_ALIGN;
+    int sms = 0;
+    rc = current_sms(&sms);
+    if (rc != VQ_OK) return rc;
+    const vqkv::AttendPlan plan = vqkv::plan_decode(*a, sms);
+    if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return VQ_ERR_WORKSPACE;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (vqkv::decode_step_supported(*a) == VQ_OK)
+        return vqkv::launch_decode(*a, plan, st, k_new_f16, v_new_f16) == cudaSuccess ? VQ_OK
+                                                                                 : VQ_ERR_CUDA;
+    // other shapes: the appends and the attention as separate launches
+    const int cap = a->kv_stride > 0 ? a->kv_stride : a->S_kv;
+    const int off = a->S_kv - a->S_q;
+    rc = encode_common(k_new_f16, a->B, a->H_kv, a->S_q, a->D, a->k_codebook, a->k_n_centroids,
+                       a->k_sub_dim, a->smooth, a->smooth_mode, const_cast<void *>(a->k_codes),
+                       in->k_code_bytes, cap, off, nullptr, 1, stream);
+    if (rc != VQ_OK) return rc;
+    rc = encode_common(v_new_f16, a->B, a->H_kv, a->S_q, a->D, a->v_codebook, a->v_n_centroids,
+                       a->v_sub_dim, nullptr, 0, const_cast<void *>(a->v_codes),
+                       in->v_code_bytes, cap, off, nullptr, 0, stream);
+    if (rc != VQ_OK) return rc;
+    return vqkv::launch_decode(*a, plan, st) == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
 int vq_prefill_attend(const vq_attend_args *in, void *stream) {
     if (!in) return VQ_ERR_NULL;
     const vq_attend_args n = vqkv::normalize_code_widths(*in);

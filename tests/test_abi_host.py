@@ -160,3 +160,20 @@ def test_library_has_sm103a_code(L):
     """The build targets sm_103a (the only -gencode in the build flags)."""
     assert vqbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
     assert os.path.getsize(vqbuild.LIB_PATH) > 100_000
+
+
+def test_decode_step_argument_errors(L):
+    """vq_decode_step: the attention checks, then its own, before any launch."""
+    step = lambda kn=FAKE, vn=FAKE, **kw: L.vq_decode_step(  # noqa: E731
+        ctypes.byref(_args(**kw)), kn, vn, None)
+    assert L.vq_decode_step(None, FAKE, FAKE, None) == vq.VQ_ERR_NULL
+    assert step(H_q=6, H_kv=4) == vq.VQ_ERR_SHAPE
+    assert step(S_q=101) == vq.VQ_ERR_SHAPE
+    assert step(S_q=101, causal=0) == vq.VQ_ERR_SHAPE      # new tokens are cache rows
+    assert step(D=96) == vq.VQ_ERR_UNSUPPORTED
+    assert step(kv_lens=FAKE) == vq.VQ_ERR_UNSUPPORTED
+    assert step(kn=None) == vq.VQ_ERR_NULL
+    assert step(vn=None) == vq.VQ_ERR_NULL
+    assert step(kn=FAKE_MIS) == vq.VQ_ERR_ALIGN
+    assert step(q_f16=FAKE_MIS) == vq.VQ_ERR_ALIGN
+    assert step(B=0, q_f16=0, out_f16=0, kn=None, vn=None) == vq.VQ_OK
