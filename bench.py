@@ -6,7 +6,7 @@ S_kv=32768 coded keys (uint8 K and V codes, 256x4 codebooks).  One step =
 vq_decode_attend (the split-KV kernel + its combine pass).
 
 Other workloads (--workload): decode-1seq (encode 8192 new keys + attend),
-gqa-decode-ragged, decode-append, bulk-encode, bulk-encode-packed,
+gqa-decode-ragged, gqa-decode-packed, decode-append, bulk-encode, bulk-encode-packed,
 chunked-prefill.
 
 Prints ONE JSON line (rank 0).  `value` is device-timed throughput with
@@ -57,6 +57,8 @@ METRICS = {
                       "cache + attend over 8192, B=1 H=8 D=128)", "tokens/s"),
     "gqa-decode-ragged": ("decode tokens/s (B=32 Hq=32 Hkv=8, cache lengths U[16384, 32768])",
                           "tokens/s"),
+    "gqa-decode-packed": ("decode tokens/s (B=32 Hq=32 Hkv=8 S_kv=32768, 10-bit packed key "
+                          "codes of a 1024x8 codebook, 20 B + 32 B per token-head)", "tokens/s"),
 }
 
 
@@ -66,6 +68,31 @@ def units_per_step(name, spec):
     return spec.B * spec.S_q                           # query tokens
 
 
+def _bits(n_centroids):
+    """Bits per bit-packed code: 2^bits >= n_centroids."""
+    b = 1
+    while (1 << b) < n_centroids:
+        b += 1
+    return b
+
+
+def pack_rows(codes, bits, torch):
+    """Codes [..., n] (a device tensor) as int32 rows of bit-packed codes:
+    code m at bits [m bits, (m + 1) bits) of the row's little-endian 32-bit
+    words (the cache layout of code_bytes 0)."""
+    n = codes.shape[-1]
+    words = (n * bits + 31) // 32
+    c = codes.to(torch.int64)
+    out = torch.zeros(codes.shape[:-1] + (words + 1,), dtype=torch.int64, device=codes.device)
+    for m in range(n):
+        w, sh = divmod(m * bits, 32)
+        v = c[..., m] << sh
+        out[..., w] |= v & 0xFFFFFFFF
+        out[..., w + 1] |= v >> 32
+    out = out[..., :words]
+    return (out - ((out >> 31) << 32)).to(torch.int32).contiguous()
+
+
 def algorithmic(name, spec, lens=None):
     """(dominant kernel, bound, work per launch, unit) -- the per-unit
     figures are stated with the design notes."""
@@ -73,9 +100,10 @@ def algorithmic(name, spec, lens=None):
         n_sub = spec.B * spec.H_kv * spec.enc_len * spec.n_k
         flops = 2.0 * spec.k_d * spec.k_N * n_sub     # one multiply-add per dim and candidate
         return "encode", "alu", flops, "TFLOP/s"
-    if name in ("gqa-decode", "decode-append", "gqa-decode-ragged"):
-        per_tok = spec.n_k * np.dtype(spec.k_code_dtype).itemsize + \
-            spec.n_v * np.dtype(spec.v_code_dtype).itemsize
+    if name in ("gqa-decode", "decode-append", "gqa-decode-ragged", "gqa-decode-packed"):
+        k_row = 4 * ((spec.n_k * _bits(spec.k_N) + 31) // 32) if spec.packed_keys else \
+            spec.n_k * np.dtype(spec.k_code_dtype).itemsize
+        per_tok = k_row + spec.n_v * np.dtype(spec.v_code_dtype).itemsize
         keys = spec.B * spec.S_kv if lens is None else int(np.sum(lens))
         byts = spec.H_kv * keys * per_tok + 2 * spec.B * spec.H_q * spec.S_q * spec.D * 2
         return "decode", "hbm", float(byts), "GB/s"
@@ -242,6 +270,9 @@ class Runner:
             dev["v_codes"] = torch.empty((s.B, s.H_kv, s.enc_len, s.n_v),
                                          dtype=vq.code_dtype(s.v_N), device="cuda")
             dev["k_hat"] = torch.empty_like(dev["keys"])
+        if s.packed_keys and not name.startswith("bulk-encode"):
+            # the drawn key codes as the cache stores them: 10-bit packed rows
+            dev["k_codes"] = pack_rows(dev["k_codes"], _bits(s.k_N), torch)
         if name == "decode-append":
             # the cache: buffers of `capacity` rows holding S_kv - 1 cached
             # tokens; each step writes the new token into row S_kv - 1

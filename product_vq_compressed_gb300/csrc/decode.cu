@@ -145,6 +145,52 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *w, int cb, int run0,
                    : ((w[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
 }
 
+// ---- kernel modes: generic (runtime code widths, tables of any size), fast
+// (uint8 codes, at most 256 centroids, one interleaved table at 64 KiB) and
+// packed (keys as bit-packed rows of kPackedBits-bit codes, values uint8;
+// both tables zero-padded to all 2^bits / 256 rows, one 128-byte row of
+// replicas per centroid)
+constexpr int kModeGeneric = 0, kModeFast = 1, kModePacked = 2;
+constexpr int kPackedBits = 10;
+constexpr uint32_t kPkRow = 128;   // bytes per centroid row of the packed-mode tables
+
+// largest bit offset inside its first word of the four lanes' runs
+__host__ __device__ constexpr int max_run_shift(int run) {
+    int m = 0;
+    for (int c = 0; c < 4; ++c) m = ((c * run) & 31) > m ? ((c * run) & 31) : m;
+    return m;
+}
+
+// Run of NC packed codes of lane c4 (codes [c4 NC, c4 NC + NC) of the row):
+// bits [c4 NC b, (c4 + 1) NC b) of the little-endian row of 32-bit words,
+// read as the two words holding them and shifted down to bit 0 of w[0].
+template <int NC>
+__device__ __forceinline__ void load_packed_run(const uint8_t *row, int c4, uint32_t *w) {
+    constexpr int RUN = NC * kPackedBits;
+    constexpr int ROW_WORDS = (4 * RUN + 31) / 32;
+    static_assert(RUN + max_run_shift(RUN) <= 64, "a lane's run must lie in two consecutive words");
+    static_assert(((3 * RUN) >> 5) + 1 < ROW_WORDS, "the second word must lie in the row");
+    const int b0 = c4 * RUN;
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(row) + (b0 >> 5);
+    uint32_t x0, x1;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(x0) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(x1) : "l"(p + 1));
+    const int sh = b0 & 31;
+    w[0] = __funnelshift_r(x0, x1, sh);
+    w[1] = x1 >> sh;
+}
+
+// Code i of a run loaded by load_packed_run (i is a constant once the
+// caller's loop is unrolled, so one shift or funnel shift and a mask).
+__device__ __forceinline__ uint32_t packed_code(const uint32_t *w, int i) {
+    const int b = i * kPackedBits;
+    uint32_t x;
+    if (b + kPackedBits <= 32) x = w[0] >> b;
+    else if (b >= 32) x = w[1] >> (b - 32);
+    else x = __funnelshift_r(w[0], w[1], b);
+    return x & ((1u << kPackedBits) - 1u);
+}
+
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
     asm("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -321,20 +367,24 @@ struct StepCodes {
 __device__ __forceinline__ int krow_of(int g8, int r) { return g8 + 8 * r; }
 __device__ __forceinline__ int vrow_of(int c4, int r) { return 2 * c4 + (r & 1) + 8 * (r >> 1); }
 
-template <int D, int DK, int DV, bool FAST>
+template <int D, int DK, int DV, int MODE>
 __device__ __forceinline__ void load_step(StepCodes<D, DK, DV> &sc, const uint8_t *kl,
                                           const uint8_t *vl, int j0, const DecArgs &a,
                                           int64_t ktb_rt, int64_t vtb_rt, int g8, int c4) {
     using SC = StepCodes<D, DK, DV>;
-    // uint8 codes on the fast path: strides are compile-time constants
-    const int64_t ktb = FAST ? (int64_t)(D / DK) : ktb_rt;
-    const int64_t vtb = FAST ? (int64_t)(D / DV) : vtb_rt;
+    constexpr bool FAST = MODE == kModeFast, PACKED = MODE == kModePacked;
+    // uint8 codes (fast path; values of the packed path) and packed key rows:
+    // strides are compile-time constants
+    const int64_t ktb = FAST ? (int64_t)(D / DK)
+                        : PACKED ? (int64_t)(4 * ((D / DK * kPackedBits + 31) / 32)) : ktb_rt;
+    const int64_t vtb = FAST || PACKED ? (int64_t)(D / DV) : vtb_rt;
     auto ld_k = [&](const uint8_t *p, uint32_t *w) {
         if constexpr (FAST) load_bytes<SC::NKL>(p, w);
+        else if constexpr (PACKED) load_packed_run<SC::NKL>(p, c4, w);
         else load_codes<SC::NKL>(p, a.kcb, w);
     };
     auto ld_v = [&](const uint8_t *p, uint32_t *w) {
-        if constexpr (FAST) load_bytes<SC::NVL>(p, w);
+        if constexpr (FAST || PACKED) load_bytes<SC::NVL>(p, w);
         else load_codes<SC::NVL>(p, a.vcb, w);
     };
     if (j0 + kStepKeys <= a.S_kv) {
@@ -504,13 +554,18 @@ struct UnitState {
 };
 
 // Gather of code u (a compile-time index after unrolling) of a code run.
-template <int DKV, int NC, bool FAST>
+// KEY: the run holds key codes (bit-packed on the packed path).
+template <int DKV, int NC, int MODE, bool KEY>
 __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const DecArgs &a,
                                             int cb, int N, uint32_t base, int row,
                                             const unsigned char *tab, uint32_t lane_off,
                                             uint32_t *w, int run0 = 0) {
-    if constexpr (FAST) {
+    if constexpr (MODE == kModeFast) {
         gather_sh<DKV>(row_off(words[u >> 2], u & 3, lane_off), w);
+    } else if constexpr (MODE == kModePacked) {
+        // tables padded to every representable code: no clamp
+        const uint32_t code = KEY ? packed_code(words, u) : (words[u >> 2] >> ((u & 3) * 8)) & 0xFFu;
+        gather_sh<DKV>(base + code * kPkRow, w);
     } else {
         const uint32_t code = min(code_at<NC>(words, cb, run0, u), (uint32_t)(N - 1));
         gather<DKV>(base + code * (uint32_t)row, w);
@@ -520,7 +575,7 @@ __device__ __forceinline__ void gather_code(const uint32_t *words, int u, const 
 // One 32-key step.  MASK: the step needs the per-column key bounds (the
 // first and last steps of a segment); the steps between take the unmasked
 // instantiation, in which every real column sees every key.
-template <int D, int DK, int DV, bool FAST, bool MASK, bool PERM>
+template <int D, int DK, int DV, int MODE, bool MASK, bool PERM>
 __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int j0,
                                              UnitState<D> &u, const DecArgs &a,
                                              uint32_t kbase, uint32_t vbase, int krow,
@@ -548,18 +603,18 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
             for (int r = 0; r < 2; ++r) {
                 if constexpr (DK == 4) {
                     uint32_t w[2];
-                    gather_code<4, SC::NKL, FAST>(sc.k[t][r], ks, a, a.kcb, a.Nk, kbase, krow,
+                    gather_code<4, SC::NKL, MODE, true>(sc.k[t][r], ks, a, a.kcb, a.Nk, kbase, krow,
                                                   tabs, klane, w, c4 * SC::NKL);
                     f[t][r][0] = w[0];
                     f[t][r][1] = w[1];
                 } else if constexpr (DK == 2) {
-                    gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks, a, a.kcb, a.Nk, kbase,
+                    gather_code<2, SC::NKL, MODE, true>(sc.k[t][r], 2 * ks, a, a.kcb, a.Nk, kbase,
                                                   krow, tabs, klane, &f[t][r][0], c4 * SC::NKL);
-                    gather_code<2, SC::NKL, FAST>(sc.k[t][r], 2 * ks + 1, a, a.kcb, a.Nk, kbase,
+                    gather_code<2, SC::NKL, MODE, true>(sc.k[t][r], 2 * ks + 1, a, a.kcb, a.Nk, kbase,
                                                   krow, tabs, klane, &f[t][r][1], c4 * SC::NKL);
                 } else {
                     if ((ks & 1) == 0)
-                        gather_code<8, SC::NKL, FAST>(sc.k[t][r], ks >> 1, a, a.kcb, a.Nk,
+                        gather_code<8, SC::NKL, MODE, true>(sc.k[t][r], ks >> 1, a, a.kcb, a.Nk,
                                                       kbase, krow, tabs, klane, w8[t][r],
                                                       c4 * SC::NKL);
                     f[t][r][0] = w8[t][r][2 * (ks & 1)];
@@ -638,7 +693,7 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int uu = 0; uu < SC::NVL; ++uu)
-                gather_code<DV, SC::NVL, FAST>(sc.v[t][r], uu, a, a.vcb, a.Nv, vbase, vrow,
+                gather_code<DV, SC::NVL, MODE, false>(sc.v[t][r], uu, a, a.vcb, a.Nv, vbase, vrow,
                                                tabs, vlane, &vw[r][uu * (DV / 2)],
                                                g8 * SC::NVL);
 #pragma unroll
@@ -777,9 +832,10 @@ __device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
     }
 }
 
-template <int D, int DK, int DV, bool FAST>
+template <int D, int DK, int DV, int MODE>
 __global__ void __launch_bounds__(warps_for(D) * 32, 1)
 decode_kernel(DecArgs a) {
+    constexpr bool FAST = MODE == kModeFast, PACKED = MODE == kModePacked;
     constexpr int kWarps = warps_for(D), kThreads = kWarps * 32;
     constexpr int KSTEPS = D / 16, MT = D / 16;
     constexpr int EK = 2 * DK, EV = 2 * DV;
@@ -787,16 +843,22 @@ decode_kernel(DecArgs a) {
 
     // shared memory: fp16 tables | per-warp scratch | fp32 staging
     //   fast path: one interleaved 256 x 256-byte table (keys | values);
+    //   packed path: key table (2^kPackedBits rows) then value table (256
+    //   rows), 128-byte rows, no staging;
     //   otherwise: key table (N_k rows) then value table (N_v rows)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int krow = a.k_copies * EK, vrow = a.v_copies * EV;   // replica bytes per row
+    constexpr size_t kPkKeyTab = (size_t)(1u << kPackedBits) * kPkRow;
     const size_t tab_bytes = FAST ? (size_t)0
-                                  : align16((size_t)a.Nk * krow) + align16((size_t)a.Nv * vrow);
+                             : PACKED ? kPkKeyTab + 256 * (size_t)kPkRow
+                                      : align16((size_t)a.Nk * krow) + align16((size_t)a.Nv * vrow);
     // fast path: scratch and staging first, the table at shared address
     // 65536 (the launch reserves 128 KiB, which always reaches past it)
     unsigned char *ktab = FAST ? smem_raw + (kFastTabAddr - (uint32_t)__cvta_generic_to_shared(smem_raw))
                                : smem_raw;
-    unsigned char *vtab = FAST ? ktab + 128 : smem_raw + align16((size_t)a.Nk * krow);
+    unsigned char *vtab = FAST     ? ktab + 128
+                          : PACKED ? smem_raw + kPkKeyTab
+                                   : smem_raw + align16((size_t)a.Nk * krow);
     WarpScratch<D> *scratch = reinterpret_cast<WarpScratch<D> *>(smem_raw + tab_bytes);
     float *stage = reinterpret_cast<float *>(scratch + kWarps);
     // ring path (uint8 codes in rows of 16-byte multiples): the stage
@@ -837,6 +899,30 @@ decode_kernel(DecArgs a) {
             for (int q = 0; q < 8; ++q) {
                 row[q] = wk;
                 row[8 + q] = wv;
+            }
+        }
+    } else if constexpr (PACKED) {
+        // every row of both tables: the thread's rows' centroids are loaded
+        // first, then each row's 8 chunks of 16 bytes are stored starting at
+        // chunk (lane mod 8), so the lanes of a store phase hit distinct banks
+        constexpr int kRows = (1 << kPackedBits) + 256;
+        constexpr int kPer = (kRows + kThreads - 1) / kThreads;
+        uint4 rw[kPer];
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const int c = tid + r * kThreads;
+            const int cv = c - (1 << kPackedBits);
+            rw[r] = c < a.Nk                      ? replica_chunk<DK>(a.kcbk + c * DK)
+                    : cv >= 0 && cv < a.Nv ? replica_chunk<DV>(a.vcbk + cv * DV)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const int c = tid + r * kThreads;
+            if (c < kRows) {
+                uint4 *row = reinterpret_cast<uint4 *>(smem_raw + (size_t)c * kPkRow);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) row[(q + lane) & 7] = rw[r];
             }
         }
     } else {
@@ -1060,10 +1146,10 @@ decode_kernel(DecArgs a) {
         // a step in [lo_any, hi_any] needs no per-column bounds
         auto step = [&](const SC &c, int jj) {
             if (jj >= us.lo_any && jj + kStepKeys - 1 <= us.hi_any)
-                process_step<D, DK, DV, FAST, false, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
+                process_step<D, DK, DV, MODE, false, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
                                                            g8, c4, smem_raw, klane, vlane);
             else
-                process_step<D, DK, DV, FAST, true, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
+                process_step<D, DK, DV, MODE, true, RING>(c, jj, us, a, kbase, vbase, krow, vrow,
                                                           g8, c4, smem_raw, klane, vlane);
         };
         if constexpr (RING) {
@@ -1087,10 +1173,10 @@ decode_kernel(DecArgs a) {
         } else {
         SC ca, cb;
         int j = j_first;
-        if (j < j_last) load_step<D, DK, DV, FAST>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
+        if (j < j_last) load_step<D, DK, DV, MODE>(ca, kl, vl, j, a, ktb, vtb, g8, c4);
         while (j < j_last) {
             if (j + kStepKeys < j_last)
-                load_step<D, DK, DV, FAST>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+                load_step<D, DK, DV, MODE>(cb, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
             // once per two steps (j - j_first is a multiple of 64 here): the
             // next 64 keys, kPrefetchTiles tiles ahead
             prefetch(j + kPrefetchTiles * kTile, kPfKeys);
@@ -1098,7 +1184,7 @@ decode_kernel(DecArgs a) {
             j += kStepKeys;
             if (j >= j_last) break;
             if (j + kStepKeys < j_last)
-                load_step<D, DK, DV, FAST>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
+                load_step<D, DK, DV, MODE>(ca, kl, vl, j + kStepKeys, a, ktb, vtb, g8, c4);
             step(cb, j);
             j += kStepKeys;
         }
@@ -1291,7 +1377,7 @@ combine_wide_kernel(DecArgs a, __half *__restrict__ out) {
 
 struct Tables {
     int k_copies, v_copies;
-    bool fast;
+    int mode;       // kModeGeneric, kModeFast or kModePacked
     size_t bytes;
 };
 
@@ -1325,9 +1411,16 @@ Tables choose_tables(const vq_attend_args &a) {
     const size_t mbars = ring ? (size_t)warps * ring_stages(stage, warps) * 8 + 8 : 0;
     if (a.k_code_bytes == 1 && a.v_code_bytes == 1 && a.k_n_centroids <= 256 &&
         a.v_n_centroids <= 256 && tail + mbars + 2048 <= kFastTabAddr)
-        return {128 / ek, 128 / ev, true,
+        return {128 / ek, 128 / ev, kModeFast,
                 ring ? (size_t)kRingAddr + (size_t)warps * ring_stages(stage, warps) * stage
                      : 2 * (size_t)kFastTabAddr};
+    // packed path: kPackedBits-bit packed keys of 8 dimensions, uint8 values
+    // of 4, D = 128; tables of 128-byte rows (8 / 16 replicas), no staging
+    if (a.D == 128 && a.k_sub_dim == 8 && a.v_sub_dim == 4 && a.k_code_bytes == 0 &&
+        packed_code_bits(a.k_n_centroids) == kPackedBits && a.v_code_bytes == 1 &&
+        a.v_n_centroids <= 256)
+        return {(int)kPkRow / ek, (int)kPkRow / ev, kModePacked,
+                ((size_t)1 << kPackedBits) * kPkRow + 256 * (size_t)kPkRow + scratch_bytes(a.D)};
     int kc = 128 / ek, vc = 128 / ev;
     auto total = [&](int k, int v) {
         return align16((size_t)a.k_n_centroids * k * ek) +
@@ -1341,12 +1434,19 @@ Tables choose_tables(const vq_attend_args &a) {
         else
             kc /= 2;
     }
-    return {kc, vc, false, total(kc, vc)};
+    return {kc, vc, kModeGeneric, total(kc, vc)};
 }
 
 template <int D, int DK, int DV>
 cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t stream) {
-    auto kern = tb.fast ? decode_kernel<D, DK, DV, true> : decode_kernel<D, DK, DV, false>;
+    void (*kern)(DecArgs) = tb.mode == kModeFast ? decode_kernel<D, DK, DV, kModeFast>
+                                                 : decode_kernel<D, DK, DV, kModeGeneric>;
+    if (tb.mode == kModePacked) {
+        if constexpr (D == 128 && DK == 8 && DV == 4)
+            kern = decode_kernel<D, DK, DV, kModePacked>;
+        else
+            return cudaErrorInvalidValue;
+    }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tb.bytes);
     if (err != cudaSuccess) return err;
@@ -1433,7 +1533,8 @@ int decode_supported(const vq_attend_args &a) {
     if (a.D != 32 && a.D != 64 && a.D != 128 && a.D != 256) return VQ_ERR_UNSUPPORTED;
     if (!pair_ok(a.D, a.k_sub_dim, a.v_sub_dim)) return VQ_ERR_UNSUPPORTED;
     const Tables tb = choose_tables(a);
-    if (tb.bytes > (tb.fast ? (size_t)kSmemLimit : kSmemBudget)) return VQ_ERR_UNSUPPORTED;
+    if (tb.bytes > (tb.mode == kModeFast ? (size_t)kSmemLimit : kSmemBudget))
+        return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
 }
 
@@ -1446,7 +1547,7 @@ int decode_step_supported(const vq_attend_args &a) {
     if (a.D != 128 || a.k_sub_dim != 4 || a.v_sub_dim != 4) return VQ_ERR_UNSUPPORTED;
     if (a.k_code_bytes != 1 || a.v_code_bytes != 1) return VQ_ERR_UNSUPPORTED;
     if (a.kv_lens) return VQ_ERR_UNSUPPORTED;
-    if (!choose_tables(a).fast) return VQ_ERR_UNSUPPORTED;
+    if (choose_tables(a).mode != kModeFast) return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
 }
 

@@ -28,6 +28,9 @@ Named workloads (sizes from the documented configurations):
                     uniformly in [S_kv / 2, S_kv]; seed 6
 ``bulk-encode-packed`` bulk-encode with the key codes stored as 10-bit packed
                     rows (20 bytes per token-head); the same inputs (seed 2)
+``gqa-decode-packed`` gqa-decode over a cache of 10-bit packed key codes
+                    (1024x8 key codebook, 20 bytes per token-head) and uint8
+                    value codes (256x4, 32 bytes); uniform codes; seed 7
 ==================  =========================================================
 
 Draw order (only what a workload uses): keys, values, outlier channels,
@@ -127,6 +130,10 @@ WORKLOADS = {
                             draw_codes=True),
     "decode-append": Spec("decode-append", B=1, H_q=8, H_kv=8, D=128, S_kv=8192,
                           S_enc=1, capacity=8192 + 64, seed=5, draw_codes=True),
+    "gqa-decode-packed": Spec("gqa-decode-packed", B=32, H_q=32, H_kv=8, D=128,
+                              S_kv=32768, k_N=1024, k_d=8, v_N=256, v_d=4, seed=7,
+                              draw_keys=False, draw_values=False, draw_codes=True,
+                              packed_keys=True),
     "gqa-decode-ragged": Spec("gqa-decode-ragged", B=32, H_q=32, H_kv=8, D=128,
                               S_kv=32768, seed=6, draw_keys=False,
                               draw_values=False, draw_codes=True, ragged=True),

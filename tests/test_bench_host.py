@@ -1,0 +1,49 @@
+"""Host logic of bench.py that needs no GPU: the bit packing it applies to
+drawn codes of packed-key workloads, and the algorithmic bytes it divides by.
+
+Packed layout (page "veloxquant_mlx.cache.vecinfer_cache module", storage
+of b-bit codes): code m of a token row occupies bits [m b, m b + b) of the
+row's little-endian 32-bit words.  The check below builds each row bit by
+bit in plain Python, independently of the vectorised packer.
+"""
+import numpy as np
+import torch
+
+import bench
+from product_vq_compressed_gb300.workloads import WORKLOADS
+
+
+def _row_bit_by_bit(codes, bits):
+    words = (len(codes) * bits + 31) // 32
+    out = [0] * words
+    for m, c in enumerate(codes):
+        for k in range(bits):
+            if (int(c) >> k) & 1:
+                pos = m * bits + k
+                out[pos // 32] |= 1 << (pos % 32)
+    return [w - (1 << 32) if w >= (1 << 31) else w for w in out]
+
+
+def test_pack_rows_matches_bit_by_bit_packing():
+    rng = np.random.default_rng(0)
+    for n, N in [(16, 1024), (32, 1000), (5, 8), (7, 65536), (16, 2)]:
+        bits = bench._bits(N)
+        codes = rng.integers(0, N, size=(3, 2, n))
+        codes[0, 0, :] = N - 1
+        got = bench.pack_rows(torch.from_numpy(codes), bits, torch).numpy()
+        assert got.dtype == np.int32
+        for idx in np.ndindex(codes.shape[:-1]):
+            assert got[idx].tolist() == _row_bit_by_bit(codes[idx], bits), (n, N, idx)
+
+
+def test_bits_per_code():
+    assert [bench._bits(n) for n in (2, 3, 4, 256, 257, 1000, 1024, 1025)] == \
+        [1, 2, 2, 8, 9, 10, 10, 11]
+
+
+def test_packed_decode_algorithmic_bytes():
+    """20-byte packed key rows + 32-byte value rows per token-head, plus q and out."""
+    s = WORKLOADS["gqa-decode-packed"]
+    _, bound, byts, unit = bench.algorithmic("gqa-decode-packed", s)
+    assert bound == "hbm" and unit == "GB/s"
+    assert byts == s.B * s.H_kv * s.S_kv * (20 + 32) + 2 * s.B * s.H_q * s.S_q * s.D * 2

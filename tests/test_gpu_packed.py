@@ -106,8 +106,11 @@ def test_encode_into_packed_rows():
 
 @pytest.mark.parametrize("Nk,dk,Nv,dv,S_q,entry", [(1024, 8, 16, 4, 1, "decode"),
                                                    (1000, 4, 256, 4, 3, "decode"),
+                                                   (1024, 8, 256, 4, 1, "decode"),
+                                                   (600, 8, 200, 4, 2, "decode"),
                                                    (256, 4, 256, 4, 128, "prefill"),
-                                                   (1024, 8, 100, 4, 80, "prefill")])
+                                                   (1024, 8, 100, 4, 80, "prefill"),
+                                                   (1024, 8, 256, 4, 80, "prefill")])
 def test_attend_over_packed_cache(Nk, dk, Nv, dv, S_q, entry):
     rng = np.random.default_rng(Nk + Nv + S_q)
     B, H_kv, H_q, D, S_kv = 2, 2, 4, 128, 300
@@ -125,5 +128,50 @@ def test_attend_over_packed_cache(Nk, dk, Nv, dv, S_q, entry):
     torch.cuda.synchronize()
     ref = oracle.attend(q, kc, kcb, vc, vcb, smooth, 1 / np.sqrt(D), True, 0)
     ok, err, _ = parity.allclose_report(out.cpu().numpy().astype(np.float64),
+                                        oracle.to_f16(ref).astype(np.float64))
+    assert ok, f"max |err| {err}"
+
+
+def _oracle_per_batch(q, kc, vc, kcb, vcb, smooth, scale, window, lens):
+    out = np.zeros(q.shape, np.float64)
+    for b, L in enumerate(lens):
+        out[b] = oracle.attend(q[b:b + 1], kc[b:b + 1, :, :L], kcb, vc[b:b + 1, :, :L], vcb,
+                               smooth, scale, True, window)[0]
+    return out
+
+
+@pytest.mark.parametrize("S_q,window,Nk", [(1, 0, 1024), (1, 300, 1024), (4, 100, 777)])
+def test_packed_key_path_gqa_window_lengths(S_q, window, Nk):
+    """The packed-key decode path (10-bit key codes of 8 dimensions, uint8
+    value codes of 4, D = 128): GQA, sliding window, per-batch lengths, a
+    buffer of more rows than S_kv, codes at both ends of the code range,
+    a ragged last tile, against the oracle on each batch's compact cache."""
+    rng = np.random.default_rng(Nk + window + S_q)
+    B, H_kv, H_q, D, dk, dv, Nv = 3, 2, 8, 128, 8, 4, 256
+    S_kv, rows = 1000, 1037
+    kcb = rng.standard_normal((Nk, dk)).astype(np.float32)
+    vcb = rng.standard_normal((Nv, dv)).astype(np.float32)
+    smooth = rng.uniform(0.5, 2.0, (H_kv, D)).astype(np.float32)
+    q = rng.standard_normal((B, H_q, S_q, D)).astype(np.float16)
+    kc = rng.integers(0, Nk, size=(B, H_kv, rows, D // dk))
+    vc = rng.integers(0, Nv, size=(B, H_kv, rows, D // dv))
+    kc[:, :, ::7] = Nk - 1          # the last code in every lane position
+    kc[:, :, 3::11] = 0
+    kp = dev(pack(kc, bits_for(Nk)))
+    vp = dev(vc.astype(np.uint8))
+    lens = [S_kv, 517, 33]
+    kl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    scale = 1 / np.sqrt(D)
+    out = vq.decode_attend(dev(q), kp, dev(kcb), vp, dev(vcb), dev(smooth), scale, causal=True,
+                           sliding_window=window, s_kv=S_kv, kv_lens=kl)
+    full = vq.decode_attend(dev(q), kp, dev(kcb), vp, dev(vcb), dev(smooth), scale,
+                            causal=True, sliding_window=window, s_kv=S_kv)
+    torch.cuda.synchronize()
+    ref = _oracle_per_batch(q, kc, vc, kcb, vcb, smooth, scale, window, lens)
+    ok, err, _ = parity.allclose_report(out.cpu().numpy().astype(np.float64),
+                                        oracle.to_f16(ref).astype(np.float64))
+    assert ok, f"kv_lens max |err| {err}"
+    ref = _oracle_per_batch(q, kc, vc, kcb, vcb, smooth, scale, window, [S_kv] * B)
+    ok, err, _ = parity.allclose_report(full.cpu().numpy().astype(np.float64),
                                         oracle.to_f16(ref).astype(np.float64))
     assert ok, f"max |err| {err}"
