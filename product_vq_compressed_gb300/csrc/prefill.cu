@@ -372,50 +372,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
     const bool has_b = hq0 + 1 < (g + 1) * a.G;
     const int q0 = qt * kRows;
 
-    if (warp == kMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
-                     ::"r"(smem_u32(tmem_slot)), "r"(kPairCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kNumPairBars; ++i) {
-            const bool commit = i == kBarSA || i == kBarSB || i == kBarOA || i == kBarOB ||
-                                i == kBarVF0 || i == kBarVF1 || i == kBarDrain;
-            mbar_init(bar(i), commit ? 1u : 4u);
-        }
-        *fail = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    if (warp >= kRebuildWarp && warp < kMmaWarp) {
-        // smooth reciprocals of the group and the fp16 codebook replicas
-        // (row c = key centroid c x16 | value centroid c x16)
-        const int t = tid - kRebuildWarp * 32;
-        const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
-        rs[t] = a.smooth_mode != 0 ? 1.f / sp[t] : 1.f;
-        for (int c = t; c < 256; c += 128) {
-            uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
-            if (c < a.Nk) {
-                const float4 f = *reinterpret_cast<const float4 *>(a.kcb + c * kSub);
-                k0 = pack_h2(f.x, f.y);
-                k1 = pack_h2(f.z, f.w);
-            }
-            if (c < a.Nv) {
-                const float4 f = *reinterpret_cast<const float4 *>(a.vcb + c * kSub);
-                v0 = pack_h2(f.x, f.y);
-                v1 = pack_h2(f.z, f.w);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
-                sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
     // ---- key tiles visible to some row of the tile (shared by both heads;
     //      batch b holds L keys)
     const int L = a.kv_lens ? min(max(a.kv_lens[b], 0), a.S_kv) : a.S_kv;
@@ -445,22 +401,75 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
         vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
     };
 
-    if (warp < kRebuildWarp && (warp < 4 || has_b)) {
-        // ---- Q~ row r of head h (fp16, swizzled A operand): each half's
-        //      butterflies below 64 in registers, the first half parked in
-        //      the K~ / V_hat region (free until the loop), then the stage
-        //      h = 64 pairs the halves: x[i], x[i + 64] -> sum, difference.
-        const int h = warp >> 2, r = tid & (kRows - 1), row = q0 + r;
-        float *xs = reinterpret_cast<float *>(gbase + 2 * kTileBytes) + h * (kD / 2) * kRows;
-        const __half *qp = a.q + (((int64_t)b * a.H_q + hq0 + h) * a.S_q + row) * kD;
-        float x[kD / 2];
+    // ---- prologue, the roles side by side: the MMA warp allocates tensor
+    //      memory and sets up the barriers; the rebuild warps start the first
+    //      tile's code loads, then build the codebook replicas; the softmax
+    //      warps build Q~ (their own smooth reciprocals)
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kPairCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+        if (lane == 0) {
+            for (int i = 0; i < kNumPairBars; ++i) {
+                const bool commit = i == kBarSA || i == kBarSB || i == kBarOA || i == kBarOB ||
+                                    i == kBarVF0 || i == kBarVF1 || i == kBarDrain;
+                mbar_init(bar(i), commit ? 1u : 4u);
+            }
+            *fail = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        }
+    } else if (warp >= kRebuildWarp) {
+        // codes of the first tile (in flight during the table build), then
+        // the fp16 codebook replicas (row c = key centroid c x16 | value
+        // centroid c x16)
+        const int t = tid - kRebuildWarp * 32;
+        if (n_tiles > 0) load_codes(t_first * kKeys, t);
+        for (int c = t; c < 256; c += 128) {
+            uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
+            if (c < a.Nk) {
+                const float4 f = *reinterpret_cast<const float4 *>(a.kcb + c * kSub);
+                k0 = pack_h2(f.x, f.y);
+                k1 = pack_h2(f.z, f.w);
+            }
+            if (c < a.Nv) {
+                const float4 f = *reinterpret_cast<const float4 *>(a.vcb + c * kSub);
+                v0 = pack_h2(f.x, f.y);
+                v1 = pack_h2(f.z, f.w);
+            }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            if (row < a.S_q) {
+            for (int q = 0; q < 8; ++q) {
+                sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
+                sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
+            }
+        }
+    } else {
+        // smooth reciprocals of the group (threads of head A), shared by
+        // the eight softmax warps through a named barrier
+        if (tid < kD) {
+            const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * kD : a.smooth;
+            rs[tid] = a.smooth_mode != 0 ? 1.f / sp[tid] : 1.f;
+        }
+        asm volatile("bar.sync 1, 256;\n" ::: "memory");
+        if (warp < 4 || has_b) {
+            // ---- Q~ row r of head h (fp16, swizzled A operand): each half's
+            //      butterflies below 64 in registers, the first half parked in
+            //      the K~ / V_hat region (free until the loop), then the stage
+            //      h = 64 pairs the halves: x[i], x[i + 64] -> sum, difference.
+            const int h = warp >> 2, r = tid & (kRows - 1), row = q0 + r;
+            float *xs = reinterpret_cast<float *>(gbase + 2 * kTileBytes) + h * (kD / 2) * kRows;
+            const __half *qp = a.q + (((int64_t)b * a.H_q + hq0 + h) * a.S_q + row) * kD;
+            // both halves' loads in flight before the first butterflies
+            uint4 raw[kD / 8];
+#pragma unroll
+            for (int e = 0; e < kD / 8; ++e)
+                raw[e] = row < a.S_q ? *reinterpret_cast<const uint4 *>(qp + 8 * e)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            float x[kD / 2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
                 for (int e = 0; e < kD / 2; e += 8) {
-                    const uint4 raw4 = *reinterpret_cast<const uint4 *>(qp + half * 64 + e);
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw4);
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw[(half * 64 + e) / 8]);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const float2 f = __half22float2(h2[k]);
@@ -468,36 +477,34 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                         x[e + 2 * k + 1] = f.y * rs[half * 64 + e + 2 * k + 1];
                     }
                 }
-            } else {
+                fwht64(x);
+                if (half == 0) {
 #pragma unroll
-                for (int e = 0; e < kD / 2; ++e) x[e] = 0.f;
+                    for (int e = 0; e < kD / 2; ++e) xs[e * kRows + r] = x[e];
+                }
             }
-            fwht64(x);
-            if (half == 0) {
+            const uint32_t sQh = sQ + (uint32_t)h * kTileBytes;
 #pragma unroll
-                for (int e = 0; e < kD / 2; ++e) xs[e * kRows + r] = x[e];
+            for (int ch = 0; ch < 8; ++ch) {
+                float lo8[8], hi8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float u = xs[(ch * 8 + k) * kRows + r], v = x[ch * 8 + k];
+                    lo8[k] = (u + v) * a.qscale;
+                    hi8[k] = (u - v) * a.qscale;
+                }
+                sts128(sQh + sw_off(r, ch), pack_h2(lo8[0], lo8[1]), pack_h2(lo8[2], lo8[3]),
+                       pack_h2(lo8[4], lo8[5]), pack_h2(lo8[6], lo8[7]));
+                sts128(sQh + sw_off(r, 8 + ch), pack_h2(hi8[0], hi8[1]), pack_h2(hi8[2], hi8[3]),
+                       pack_h2(hi8[4], hi8[5]), pack_h2(hi8[6], hi8[7]));
             }
+            fence_proxy_async();
         }
-        const uint32_t sQh = sQ + (uint32_t)h * kTileBytes;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            float lo8[8], hi8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float u = xs[(ch * 8 + k) * kRows + r], v = x[ch * 8 + k];
-                lo8[k] = (u + v) * a.qscale;
-                hi8[k] = (u - v) * a.qscale;
-            }
-            sts128(sQh + sw_off(r, ch), pack_h2(lo8[0], lo8[1]), pack_h2(lo8[2], lo8[3]),
-                   pack_h2(lo8[4], lo8[5]), pack_h2(lo8[6], lo8[7]));
-            sts128(sQh + sw_off(r, 8 + ch), pack_h2(hi8[0], hi8[1]), pack_h2(hi8[2], hi8[3]),
-                   pack_h2(hi8[4], hi8[5]), pack_h2(hi8[6], hi8[7]));
-        }
-        fence_proxy_async();
-    } else if (warp < kMmaWarp && n_tiles > 0) {
-        load_codes(t_first * kKeys, tid - kRebuildWarp * 32);
     }
-    __syncthreads();   // Q~ written, the scratch region free
+    tc_fence_before();
+    __syncthreads();   // tensor memory, barriers, tables and Q~ ready; scratch free
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
     // softmax role: head h, row r (tensor-memory lane r)
     const int h = (warp >> 2) & 1, r = tid & (kRows - 1), row = q0 + r;
@@ -719,15 +726,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
         }
         __syncwarp();
     }
-    tc_fence_before();
-    __syncthreads();   // every role has left its loop; every product has completed
-    tc_fence_after();
-
     if (warp < kRebuildWarp && (h == 0 || has_b)) {
-        // ---- output row r of head h (tcgen05.ld is warp-collective: every
-        //      lane loads, only rows of the query block are stored)
+        // ---- output row r of head h, as soon as the head's last P V_hat has
+        //      completed (the other head's last tile may still be running).
+        //      Its completion is phase n_tiles - 1 of the head's O barrier:
+        //      this warp saw S(last) complete, which was issued only after
+        //      phase n_tiles - 2 had completed, so the parity wait cannot
+        //      match an earlier phase.  (tcgen05.ld is warp-collective: every
+        //      lane loads, only rows of the query block are stored.)
+        bool have_o = n_tiles > 0 && *fail == 0;
+        if (have_o) have_o = warp_wait(bar(kBarOA + h), (uint32_t)((n_tiles - 1) & 1), fail);
+        tc_fence_after();
         const bool failed = *fail != 0;
-        const bool have_o = n_tiles > 0 && !failed;
+        have_o = have_o && !failed;
         const float inv = failed ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
         __half *op = a.out + (((int64_t)b * a.H_q + hq0 + h) * a.S_q + row) * kD;
 #pragma unroll 1
