@@ -25,7 +25,10 @@
 // Every mbarrier wait is bounded: if one expires the CTA writes NaN rows,
 // waits (bounded) for its own MMAs once more, frees its tensor memory and
 // exits, so a fault shows up in the output instead of hanging the GPU.
+#include <cuda.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "vq_internal.cuh"
 
@@ -38,7 +41,10 @@ constexpr int kD = 128;           // head dimension of this kernel
 constexpr int kSub = 4;           // sub-vector size of both codebooks
 constexpr uint32_t kTileBytes = kRows * kD * 2;  // one fp16 operand tile, 32 KiB
 constexpr uint32_t kHalfTile = kTileBytes / 2;   // 64-element K half, 16 KiB
-constexpr uint32_t kTabBytes = 256 * 256;        // interleaved K | V replicas
+constexpr uint32_t kTabKBytes = 256 * 128;       // key centroids: 16 fp16 replicas per row
+constexpr uint32_t kTabVBytes = 256 * 64;        // value centroids: 8 fp16 replicas per row
+constexpr uint32_t kCodeTile = kKeys * 32;       // one tile's K (or V) codes, 4 KiB
+constexpr uint32_t kStageBytes = 2 * kCodeTile;  // a ring stage: K codes | V codes
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr float kSlack = 8.f;     // base-2 headroom of a row's reference maximum
 
@@ -204,6 +210,8 @@ enum PairBar {
     kBarV0, kBarV1,       // V_hat buffer 0 / 1 written (one arrival per warp)
     kBarVF0, kBarVF1,     // V_hat buffer 0 / 1 free again (commit)
     kBarDrain,            // every issued product complete (commit)
+    kBarC0, kBarC1,       // code stage 0 / 1 loaded (tensor copies, transaction bytes)
+    kBarE0, kBarE1,       // code stage 0 / 1 read (one arrival per rebuild warp)
     kNumPairBars
 };
 
@@ -347,15 +355,42 @@ __device__ __forceinline__ void fwht64(float *x) {
     }
 }
 
-__global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillArgs a) {
+// One tile of code rows (128 rows of 32 bytes, starting at row `row` of the
+// tensor map's [rows x 32 bytes] view of a code buffer) into shared memory by
+// the tensor copy engine, completing on `bar` (rows past the buffer read as
+// zero).  The innermost coordinate is 0: 16-byte aligned.
+__device__ __forceinline__ void tma_code_tile(uint32_t dst, const CUtensorMap *map, int row,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+prefill_pair_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte aligned: Q~_A | Q~_B | K~ | V_hat 0 | V_hat 1 | tables | misc
+    // 1024-byte aligned: Q~_A | Q~_B | K~ | V_hat 0 | V_hat 1 | key table |
+    // value table | code ring (2 stages) | misc
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t sQ = base, sK = base + 2 * kTileBytes, sV = base + 3 * kTileBytes,
-                   sTab = base + 5 * kTileBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + 5 * kTileBytes + kTabBytes);
+                   sTabK = base + 5 * kTileBytes, sTabV = sTabK + kTabKBytes,
+                   sRing = sTabV + kTabVBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + (sRing - base) + 2 * kStageBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumPairBars);
     volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *rs = reinterpret_cast<float *>(tmem_slot + 2);   // [kD] 1 / s_g
@@ -385,21 +420,20 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
     const int t_last = cta_hi < cta_lo ? t_first - 1 : cta_hi / kKeys;   // none: empty range
     const int n_tiles = t_last - t_first + 1;
 
+    // code tiles come from a ring of two stages filled by the tensor copy
+    // engine: tile t_first + i in stage i mod 2, its copy issued (by the
+    // first rebuild thread) once every rebuild warp has read tile i - 2
     const int64_t bg = (int64_t)b * a.H_kv + g;
-    const uint8_t *kcodes = a.kc + bg * a.stride * 32;
-    const uint8_t *vcodes = a.vc + bg * a.stride * 32;
-    uint32_t kcw[8], vcw[8];   // rebuild role: the 32 K and V codes of its key row
-    auto load_codes = [&](int j0, int r) {
-        const int j = min(j0 + r, a.S_kv - 1);
-        const uint4 c0 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4 *>(kcodes + (int64_t)j * 32 + 16);
-        const uint4 d0 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32);
-        const uint4 d1 = *reinterpret_cast<const uint4 *>(vcodes + (int64_t)j * 32 + 16);
-        kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
-        kcw[4] = c1.x; kcw[5] = c1.y; kcw[6] = c1.z; kcw[7] = c1.w;
-        vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
-        vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
+    const int code_row0 = (int)(bg * a.stride);   // tensor-map row of key 0 of (b, g)
+    const bool producer = tid == kRebuildWarp * 32;
+    auto issue_codes = [&](int tile) {   // producer only
+        const int st = (tile - t_first) & 1;
+        const uint32_t dst = sRing + (uint32_t)st * kStageBytes;
+        mbar_expect_tx(bar(kBarC0 + st), kStageBytes);
+        tma_code_tile(dst, &tm_k, code_row0 + tile * kKeys, bar(kBarC0 + st));
+        tma_code_tile(dst + kCodeTile, &tm_v, code_row0 + tile * kKeys, bar(kBarC0 + st));
     };
+    uint32_t kcw[8], vcw[8];   // rebuild role: the 32 K and V codes of its key row
 
     // ---- prologue, the roles side by side: the MMA warp allocates tensor
     //      memory and sets up the barriers; the rebuild warps start the first
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                      ::"r"(smem_u32(tmem_slot)), "r"(kPairCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
         if (lane == 0) {
-            for (int i = 0; i < kNumPairBars; ++i) {
+            for (int i = 0; i < kBarC0; ++i) {
                 const bool commit = i == kBarSA || i == kBarSB || i == kBarOA || i == kBarOB ||
                                     i == kBarVF0 || i == kBarVF1 || i == kBarDrain;
                 mbar_init(bar(i), commit ? 1u : 4u);
@@ -419,11 +453,23 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         }
     } else if (warp >= kRebuildWarp) {
-        // codes of the first tile (in flight during the table build), then
-        // the fp16 codebook replicas (row c = key centroid c x16 | value
-        // centroid c x16)
+        // the copies of the first two tiles' codes (in flight during the
+        // table build), then the fp16 codebook replicas: key table row c =
+        // centroid c x16, value table row c = centroid c x8
         const int t = tid - kRebuildWarp * 32;
-        if (n_tiles > 0) load_codes(t_first * kKeys, t);
+        if (producer) {
+            // the ring's barriers, then the first two tiles' copies
+            mbar_init(bar(kBarC0), 1u);
+            mbar_init(bar(kBarC1), 1u);
+            mbar_init(bar(kBarE0), 4u);
+            mbar_init(bar(kBarE1), 4u);
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+            fence_proxy_async();
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+            if (n_tiles > 0) issue_codes(t_first);
+            if (n_tiles > 1) issue_codes(t_first + 1);
+        }
         for (int c = t; c < 256; c += 128) {
             uint32_t k0 = 0u, k1 = 0u, v0 = 0u, v1 = 0u;
             if (c < a.Nk) {
@@ -437,10 +483,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                 v1 = pack_h2(f.z, f.w);
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                sts128(sTab + (uint32_t)c * 256u + q * 16u, k0, k1, k0, k1);
-                sts128(sTab + (uint32_t)c * 256u + 128u + q * 16u, v0, v1, v0, v1);
-            }
+            for (int q = 0; q < 8; ++q) sts128(sTabK + (uint32_t)c * 128u + q * 16u, k0, k1, k0, k1);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sts128(sTabV + (uint32_t)c * 64u + q * 16u, v0, v1, v0, v1);
         }
     } else {
         // smooth reciprocals of the group (threads of head A), shared by
@@ -614,26 +659,54 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
     } else if (warp < kMmaWarp) {
         // ================= rebuild of K~ and V_hat, key row r of each tile
         const int r = tid - kRebuildWarp * 32;
-        const uint32_t lane_off = (uint32_t)((lane & 15) * 8);
-        auto build_row = [&](const uint32_t *cw, uint32_t dst, uint32_t side) {
+        // gather address of code byte i of word w: a byte permute gives
+        // code * 256 + o, shifted down to the table's row size -- key rows of
+        // 128 bytes (the lane's replica (lane mod 16) * 8, o = 2x that),
+        // value rows of 64 bytes (replica (lane mod 8) * 8, o = 4x that)
+        const uint32_t ok2 = (uint32_t)((lane & 15) * 16), ov4 = (uint32_t)((lane & 7) * 32);
+        auto build_row = [&](const uint32_t *cw, uint32_t dst, uint32_t tab, uint32_t o, int sh) {
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
                 const uint32_t w = cw[ch >> 1];
                 const uint32_t i0 = (uint32_t)(ch & 1) * 2u;
-                const uint32_t o = side + lane_off;
-                const uint2 e0 = lds64(sTab + __byte_perm(w, o, 0x6504u | (i0 << 4)));
-                const uint2 e1 = lds64(sTab + __byte_perm(w, o, 0x6504u | ((i0 + 1u) << 4)));
+                const uint2 e0 = lds64(tab + (__byte_perm(w, o, 0x6504u | (i0 << 4)) >> sh));
+                const uint2 e1 = lds64(tab + (__byte_perm(w, o, 0x6504u | ((i0 + 1u) << 4)) >> sh));
                 sts128(dst + sw_off(r, ch), e0.x, e0.y, e1.x, e1.y);
             }
         };
         uint32_t ph_sb = 0, ph_vf = 0;   // ph_vf: bit b = parity of V_hat buffer b
+        int issued = n_tiles > 1 ? t_first + 1 : t_last;   // last tile whose copy was issued
+        int consumed = t_first - 1;                           // last tile read from the ring
         for (int tile = t_first; tile <= t_last; ++tile) {
-            const int i = tile - t_first;
+            const int i = tile - t_first, st = i & 1;
+            // this tile's codes (row r of its stage), then the stage back to
+            // the producer, which refills it with tile + 2
+            if (!warp_wait(bar(kBarC0 + st), (uint32_t)((i >> 1) & 1), fail)) break;
+            consumed = tile;
+            {
+                const uint32_t src = sRing + (uint32_t)st * kStageBytes + (uint32_t)r * 32u;
+                const uint4 c0 = lds128(src), c1 = lds128(src + 16);
+                const uint4 d0 = lds128(src + kCodeTile), d1 = lds128(src + kCodeTile + 16);
+                kcw[0] = c0.x; kcw[1] = c0.y; kcw[2] = c0.z; kcw[3] = c0.w;
+                kcw[4] = c1.x; kcw[5] = c1.y; kcw[6] = c1.z; kcw[7] = c1.w;
+                vcw[0] = d0.x; vcw[1] = d0.y; vcw[2] = d0.z; vcw[3] = d0.w;
+                vcw[4] = d1.x; vcw[5] = d1.y; vcw[6] = d1.z; vcw[7] = d1.w;
+            }
+            warp_arrive(bar(kBarE0 + st));
+            if (warp == kRebuildWarp && tile + 2 <= t_last) {
+                if (!warp_wait(bar(kBarE0 + st), (uint32_t)((i >> 1) & 1), fail)) break;
+                if (producer) {
+                    fence_proxy_async();   // the stage's reads before the copy's writes
+                    issue_codes(tile + 2);
+                }
+                issued = tile + 2;
+                __syncwarp();
+            }
             if (i > 0) {   // the score blocks of the previous tile read K~
                 if (!warp_wait(bar(has_b ? kBarSB : kBarSA), ph_sb, fail)) break;
                 ph_sb ^= 1;
             }
-            build_row(kcw, sK, 0u);
+            build_row(kcw, sK, sTabK, ok2, 1);
             fence_proxy_async();
             warp_arrive(bar(kBarK));
             const int vb = i & 1;
@@ -641,10 +714,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
                 if (!warp_wait(bar(kBarVF0 + vb), (ph_vf >> vb) & 1u, fail)) break;
                 ph_vf ^= 1u << vb;
             }
-            build_row(vcw, sV + (uint32_t)vb * kTileBytes, 128u);
+            build_row(vcw, sV + (uint32_t)vb * kTileBytes, sTabV, ov4, 2);
             fence_proxy_async();
             warp_arrive(bar(kBarV0 + vb));
-            if (tile < t_last) load_codes((tile + 1) * kKeys, r);
+        }
+        // after a failure: the producer's warp waits (bounded, whatever the
+        // failure flag) for its copies still in flight before the CTA can end
+        if (warp == kRebuildWarp) {
+            for (int tile = consumed + 1; tile <= issued; ++tile) {
+                const int i = tile - t_first;
+                bool done = false;
+                for (uint32_t it = 0; it < kWaitLimit && !done; ++it)
+                    done = __all_sync(0xffffffffu, mbar_try(bar(kBarC0 + (i & 1)), (uint32_t)((i >> 1) & 1)));
+            }
         }
         __syncwarp();
     } else {
@@ -774,8 +856,42 @@ __global__ void __launch_bounds__(kPairThreads, 1) prefill_pair_kernel(PrefillAr
 }
 
 size_t prefill_pair_smem_bytes() {
-    return 5 * (size_t)kTileBytes + kTabBytes + kNumPairBars * 8 + 8 + kD * sizeof(float) +
-           1024;   // + alignment slack
+    return 5 * (size_t)kTileBytes + kTabKBytes + kTabVBytes + 2 * (size_t)kStageBytes +
+           kNumPairBars * 8 + 8 + kD * sizeof(float) + 1024;   // + alignment slack
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// links no driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of a uint8 code buffer seen as [rows x 32 bytes]; tiles of
+// 128 rows.
+bool code_tensor_map(CUtensorMap *m, const void *codes, uint64_t rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {32, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {32};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kKeys};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(codes), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -785,6 +901,9 @@ int prefill_supported(const vq_attend_args &a) {
     if (a.k_code_bytes != 1 || a.v_code_bytes != 1) return VQ_ERR_UNSUPPORTED;
     if (a.k_n_centroids > 256 || a.v_n_centroids > 256) return VQ_ERR_UNSUPPORTED;
     if (a.S_q < 64) return VQ_ERR_UNSUPPORTED;
+    // code tiles are addressed by 32-bit tensor-map row coordinates
+    const int64_t stride = a.kv_stride > 0 ? a.kv_stride : a.S_kv;
+    if ((int64_t)a.B * a.H_kv * stride + kKeys >= ((int64_t)1 << 31)) return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
 }
 
@@ -813,8 +932,12 @@ cudaError_t launch_prefill(const vq_attend_args &a, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(prefill_pair_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    CUtensorMap tmk, tmv;
+    const uint64_t rows = (uint64_t)a.B * a.H_kv * (uint64_t)p.stride;
+    if (!code_tensor_map(&tmk, a.k_codes, rows) || !code_tensor_map(&tmv, a.v_codes, rows))
+        return cudaErrorInvalidValue;
     dim3 grid(q_tiles, (unsigned)(a.H_kv * ((p.G + 1) / 2)), (unsigned)a.B);
-    prefill_pair_kernel<<<grid, kPairThreads, smem, stream>>>(p);
+    prefill_pair_kernel<<<grid, kPairThreads, smem, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,8 @@ CASES = [
     (1, 2, 1, 4101, 96, True, 1000, 2),    # long cache, window
     (1, 4, 4, 333, 130, True, 0, 0),       # group 1: single-head CTAs
     (1, 6, 2, 450, 256, True, 129, 2),     # group 3: a pair and a single head
+    (1, 4, 1, 2000, 384, True, 200, 2),    # three query tiles: the last CTA pair half empty
+    (2, 4, 2, 1500, 640, False, 300, 2),   # five query tiles, window, not causal
 ]
 
 
