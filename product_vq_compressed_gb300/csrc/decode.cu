@@ -707,16 +707,23 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
     }
 }
 
-// Encode of one new token by one warp, D = 32 E with sub-vectors of E
-// dimensions (lane m owns sub-vector m), into its 32-byte uint8 code row
-// (cb: the fp32 codebook, staged in shared memory by the caller):
-// the same definition and decision rule as the encode kernels -- smooth and
+// Encode of one new token by a group of NW warps, D = 32 E with sub-vectors
+// of E dimensions (lane m owns sub-vector m), into its 32-byte uint8 code row
+// (cb: the fp32 codebook, staged in shared memory by the caller): the same
+// definition and decision rule as the encode kernels -- smooth and
 // Walsh-Hadamard rotation (keys), nearest centroid by the direct-form fp32
 // distance to every centroid, lowest index on ties, kept when the rounding
-// certificate holds and decided again in float-float otherwise.
-template <int E>
-__device__ void encode_token_warp(const __half *x, const float *sm, int rotate, const float *cb,
-                                  int N, uint8_t *dst, int log2D, int lane) {
+// certificate holds and decided again in float-float otherwise.  Warp `part`
+// of the group scans centroids [part N / NW, (part + 1) N / NW) and leaves
+// its best, second-best and index per lane in its exchange area (3 x 32
+// words at xch + part * xstride); after the group's named barrier `bar_id`
+// the group's first warp
+// combines them in part order (so an equal distance keeps the lower index),
+// takes the decision and writes the row.
+template <int E, int NW>
+__device__ void encode_token_group(const __half *x, const float *sm, int rotate, const float *cb,
+                                   int N, uint8_t *dst, int log2D, int lane, int part,
+                                   float *xch, int xstride, int bar_id) {
     const float inv_sqrt_d = 1.f / sqrtf((float)(32 * E));
     float f[E];
     load_halves<E>(x + lane * E, f);
@@ -740,8 +747,9 @@ __device__ void encode_token_warp(const __half *x, const float *sm, int rotate, 
     const float delta = rotate ? asum * rotation_delta_coef(log2D, inv_sqrt_d) : 0.f;
     float b = INFINITY, b2 = INFINITY;
     int bi = 0;
+    const int c_lo = part * N / NW, c_hi = (part + 1) * N / NW;
 #pragma unroll 8
-    for (int c = 0; c < N; ++c) {
+    for (int c = c_lo; c < c_hi; ++c) {
         float cv[E];
         load_floats<E>(cb + (size_t)c * E, cv);
         float d = 0.f;
@@ -752,6 +760,29 @@ __device__ void encode_token_warp(const __half *x, const float *sm, int rotate, 
         }
         b2 = fminf(b2, fmaxf(b, d));
         if (d < b) { b = d; bi = c; }
+    }
+    if constexpr (NW > 1) {
+        float *mine = xch + part * xstride;
+        mine[lane] = b;
+        mine[32 + lane] = b2;
+        mine[64 + lane] = __int_as_float(bi);
+        asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(NW * 32) : "memory");
+        if (part != 0) {
+            // the others' values are read before any warp of the group
+            // moves on to another token
+            asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(NW * 32) : "memory");
+            return;
+        }
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+            const float *theirs = xch + w * xstride;
+            const float bw = theirs[lane], b2w = theirs[32 + lane];
+            const int biw = __float_as_int(theirs[64 + lane]);
+            const float nb2 = fminf(fminf(b2, b2w), fmaxf(b, bw));
+            if (bw < b) { b = bw; bi = biw; }
+            b2 = nb2;
+        }
+        asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(NW * 32) : "memory");
     }
     int code = bi;
     unsigned m = __ballot_sync(0xffffffffu, !code_certified<E>(b, b2, delta));
@@ -768,13 +799,15 @@ __device__ void encode_token_warp(const __half *x, const float *sm, int rotate, 
 
 // Merge of the key splits inside a decode step (after the grid sync): CTA
 // c takes the (unit, column, 32 output dimensions) items c, c + grid, ...;
-// its warps split the item's records, each lane one output dimension; the
-// maxima, sums and partial outputs are reduced in shared memory (`sm` >=
+// its warps split the item's records, each lane one output dimension: a
+// warp folds its records (a batch loaded at once) into a running (m, l, o),
+// and the warps' (m, l, o) are combined in shared memory (`sm` >=
 // (32 kWarps + 2 kWarps) floats), out = o / l in fp16.
 template <int D, int kWarps>
 __device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
-    float *part = sm;                      // [kWarps][32]
-    float *red = sm + kWarps * 32;         // [2][kWarps]
+    float *part = sm;                      // [kWarps][32]: each warp's o
+    float *red = sm + kWarps * 32;         // [kWarps][2]: each warp's (m, l)
+    constexpr int kBatch = 16;             // records a warp loads at once
     const int64_t units = a.total / a.T;
     const int ncb = min(kCols, a.G * a.S_q);
     constexpr int nch = D / 32;
@@ -788,38 +821,58 @@ __device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
         int64_t w_lo;
         int n_rec;
         unit_warps(a, unit, &w_lo, &n_rec);
-        // maximum over the records
-        float M = -INFINITY;
-        for (int k = warp * 32 + lane; k < n_rec; k += kWarps * 32)
-            M = fmaxf(M, __ldcg(unit_record(a, unit, w_lo + k, col, D)));
+        // each warp: its records k = warp, warp + kWarps, ..., kBatch of them
+        // loaded at once, folded into a running (m, l, o) rescaled once per
+        // batch
+        float mw = -INFINITY, lw = 0.f, ow = 0.f;
+        for (int k0 = warp; k0 < n_rec; k0 += kWarps * kBatch) {
+            float2 ml[kBatch];
+            float ov[kBatch];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        if (lane == 0) red[warp] = M;
-        __syncthreads();
-        M = red[0];
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
-        // each warp: its records' weighted sums (every record of a warp
-        // loaded before any is used)
-        float l = 0.f, o = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int k = warp; k < n_rec; k += kWarps) {
-                const float *r = unit_record(a, unit, w_lo + k, col, D);
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(r));
-                const float ov = __ldcg(r + 4 + ch * 32 + lane);
-                const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-                l = fmaf(f, ml.y, l);
-                o = fmaf(f, ov, o);
+            for (int j = 0; j < kBatch; ++j) {
+                const int k = k0 + j * kWarps;
+                if (k < n_rec) {
+                    const float *r = unit_record(a, unit, w_lo + k, col, D);
+                    ml[j] = __ldcg(reinterpret_cast<const float2 *>(r));
+                    ov[j] = __ldcg(r + 4 + ch * 32 + lane);
+                } else {
+                    ml[j] = make_float2(-INFINITY, 0.f);
+                    ov[j] = 0.f;
+                }
+            }
+            float bm = mw;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) bm = fmaxf(bm, ml[j].x);
+            if (bm != -INFINITY) {
+                const float sc = mw == -INFINITY ? 0.f : exp2f(mw - bm);
+                lw *= sc;
+                ow *= sc;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const float f = ml[j].x == -INFINITY ? 0.f : exp2f(ml[j].x - bm);
+                    lw = fmaf(f, ml[j].y, lw);
+                    ow = fmaf(f, ov[j], ow);
+                }
+                mw = bm;
             }
         }
-        part[warp * 32 + lane] = o;
-        if (lane == 0) red[kWarps + warp] = l;
+        part[warp * 32 + lane] = ow;
+        if (lane == 0) {
+            red[2 * warp] = mw;
+            red[2 * warp + 1] = lw;
+        }
         __syncthreads();
         if (warp == 0) {
+            float M = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red[2 * w]);
             float lt = 0.f, acc = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                lt += red[kWarps + w];
-                acc += part[w * 32 + lane];
+            if (M != -INFINITY) {
+                for (int w = 0; w < kWarps; ++w) {
+                    const float m = red[2 * w];
+                    const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+                    lt = fmaf(f, red[2 * w + 1], lt);
+                    acc = fmaf(f, part[w * 32 + lane], acc);
+                }
             }
             const int bgi = (int)(unit / a.n_colblk);
             const int b = bgi / a.H_kv, g = bgi % a.H_kv;
@@ -836,6 +889,7 @@ template <int D, int DK, int DV, int MODE>
 __global__ void __launch_bounds__(warps_for(D) * 32, 1)
 decode_kernel(DecArgs a) {
     constexpr bool FAST = MODE == kModeFast, PACKED = MODE == kModePacked;
+    constexpr bool kStepShape = FAST && D == 128 && DK == 4 && DV == 4;   // decode-step capable
     constexpr int kWarps = warps_for(D), kThreads = kWarps * 32;
     constexpr int KSTEPS = D / 16, MT = D / 16;
     constexpr int EK = 2 * DK, EV = 2 * DV;
@@ -881,17 +935,53 @@ decode_kernel(DecArgs a) {
 
     // ---- fp16 tables replicated per bank group (rows past N are zero)
     if constexpr (FAST) {
-        // a decode step's encode reads the fp32 codebooks from the staging area
-        if (a.step) {
-            const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
-            for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
-            for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
+        int t0 = 0;   // first thread of the table build
+        if constexpr (kStepShape) {
+            if (a.step) {
+                // ---- decode step: the fp32 codebooks staged, then the new
+                //      tokens encoded into their cache rows by warps 0-3 (one
+                //      token at a time, the codebook split over the 4 warps;
+                //      tokens c, c + grid, ... on CTA c) while the other warps
+                //      build the table
+                const int nk_f = a.Nk * DK, nv_f = a.Nv * DV;
+                for (int i = tid; i < nk_f; i += kThreads) stage[i] = a.kcbk[i];
+                for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
+                __syncthreads();
+                pdl_wait();
+                constexpr int kEncWarps = 4;
+                static_assert(kThreads - kEncWarps * 32 >= 256, "one table row per builder thread");
+                t0 = kEncWarps * 32;
+                if (warp < kEncWarps) {
+                    const int n_new = a.B * a.H_kv * a.S_q;
+                    // exchange areas: the encoding warps' query scratch
+                    // (unused until the attention)
+                    float *xch = reinterpret_cast<float *>(scratch[0].qt);
+                    constexpr int kXStride = (int)(sizeof(WarpScratch<D>) / sizeof(float));
+                    static_assert(sizeof(WarpScratch<D>) % sizeof(float) == 0 &&
+                                      sizeof(scratch[0].qt) >= 96 * sizeof(float),
+                                  "exchange area of 96 words per warp");
+                    for (int task = (int)blockIdx.x; task < 2 * n_new; task += (int)gridDim.x) {
+                        const int tok = task >> 1, is_v = task & 1;
+                        const int bh = tok / a.S_q, tt = tok - bh * a.S_q;
+                        const int h = bh % a.H_kv;
+                        const __half *x = (is_v ? a.v_new : a.k_new) + (int64_t)tok * D;
+                        uint8_t *dst = const_cast<uint8_t *>(is_v ? a.vc : a.kc) +
+                                       ((int64_t)bh * a.stride + a.new_row0 + tt) * 32;
+                        const float *smr = is_v || a.smooth_mode == 0 ? nullptr
+                                           : a.smooth_mode == 2 ? a.smooth + (size_t)h * D
+                                                                : a.smooth;
+                        encode_token_group<4, kEncWarps>(
+                            x, smr, !is_v, is_v ? stage + a.Nk * DK : stage, is_v ? a.Nv : a.Nk,
+                            dst, a.log2D, lane, warp, xch, kXStride, 1);
+                    }
+                }
+            }
         }
         // 256 rows x 16 chunks of 16 bytes (8 key, 8 value); every chunk of a
         // row half holds 16 / EK (16 / EV) copies of its centroid.  A thread
         // owns whole rows: both centroid loads are in flight together, then
         // the 16 stores.
-        for (int c = tid; c < 256; c += kThreads) {
+        for (int c = tid - t0; c >= 0 && c < 256; c += kThreads - t0) {
             const uint4 wk = c < a.Nk ? replica_chunk<DK>(a.kcbk + c * DK) : make_uint4(0u, 0u, 0u, 0u);
             const uint4 wv = c < a.Nv ? replica_chunk<DV>(a.vcbk + c * DV) : make_uint4(0u, 0u, 0u, 0u);
             uint4 *row = reinterpret_cast<uint4 *>(ktab + c * kFastRow);
@@ -957,34 +1047,6 @@ decode_kernel(DecArgs a) {
     const int n_cols_total = a.G * a.S_q;
     WarpScratch<D> &ws = scratch[warp];
 
-    // ---- decode step: the new tokens' codes into the cache, then a grid sync
-    //      (every warp of the grid takes tokens; the attention below reads
-    //      them through the bulk copies, which need the proxy fence)
-    if constexpr (FAST && D == 128 && DK == 4 && DV == 4) {
-        if (a.step) {
-            const int n_new = a.B * a.H_kv * a.S_q;
-            const int gwarps = (int)gridDim.x * kWarps;
-            // tasks go to the CTAs first (task t: CTA t mod grid), so that a
-            // few tokens are encoded on as many SMs
-            for (int task = warp * (int)gridDim.x + (int)blockIdx.x; task < 2 * n_new;
-                 task += gwarps) {
-                const int tok = task >> 1, is_v = task & 1;
-                const int bh = tok / a.S_q, tt = tok - bh * a.S_q;
-                const int h = bh % a.H_kv;
-                const __half *x = (is_v ? a.v_new : a.k_new) + (int64_t)tok * D;
-                uint8_t *dst = const_cast<uint8_t *>(is_v ? a.vc : a.kc) +
-                               ((int64_t)bh * a.stride + a.new_row0 + tt) * 32;
-                const float *smr = is_v || a.smooth_mode == 0 ? nullptr
-                                   : a.smooth_mode == 2 ? a.smooth + (size_t)h * D : a.smooth;
-                encode_token_warp<4>(x, smr, !is_v, is_v ? stage + a.Nk * DK : stage,
-                                     is_v ? a.Nv : a.Nk, dst, a.log2D, lane);
-            }
-            __threadfence();
-            cooperative_groups::this_grid().sync();
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
-        }
-    }
-
     // warps past the plan's last one have no share (they still reach the
     // grid syncs of a decode step)
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
@@ -1041,13 +1103,32 @@ decode_kernel(DecArgs a) {
             pvalid = true;
             pseek();
         }
-        for (int k = 0; k < kStages; ++k) issue();
+        // in a decode step, a copy that reads the new rows [new_row0, ..)
+        // waits until they are written (the rest of the fill after the sync)
+        for (int k = 0; k < kStages; ++k) {
+            if (kStepShape && a.step && pvalid && pj + kStepKeys > a.new_row0) break;
+            issue();
+        }
     }
+    // ---- decode step: every new token's codes are in the cache (encoded
+    //      with the table build above), then a grid sync (the attention below
+    //      reads them through the bulk copies, which need the proxy fence)
+    if constexpr (kStepShape) {
+        if (a.step) {
+            __threadfence();
+            cooperative_groups::this_grid().sync();
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            if constexpr (RING) {
+                while (pvalid && issued < kStages) issue();   // nothing consumed yet
+            }
+        }
+    }
+
     int consumed = 0;
 
     while (t < t_end) {
         const SegInfo sg = segment_at(a, t, t_end);
-        const int64_t unit = sg.unit, seg_end = sg.seg_end, bg = sg.bg;
+        const int64_t seg_end = sg.seg_end, bg = sg.bg;
         const int cblk = sg.cblk, g = sg.g, b = sg.b, kv_len = sg.kv_len;
         const int j_first = sg.j_first, j_last = sg.j_last;
         // the segment's first code tiles go to L2 while the queries are prepared
@@ -1227,7 +1308,7 @@ decode_kernel(DecArgs a) {
     }
     // ---- decode step: every record written, then the merge of the splits
     //      (the codebook table region is free now)
-    if constexpr (FAST && D == 128 && DK == 4 && DV == 4) {
+    if constexpr (kStepShape) {
         if (a.step) {
             __threadfence();
             cooperative_groups::this_grid().sync();
