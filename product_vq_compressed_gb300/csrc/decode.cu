@@ -885,11 +885,16 @@ __device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
     }
 }
 
-template <int D, int DK, int DV, int MODE>
+// STEP: the single-launch decode step (vq_decode_step): the new tokens'
+// encode, the attention and the merge of the key splits, with grid syncs
+// between them (a cooperative launch); only the 128 / 4 / 4 fast
+// instantiation has it.
+template <int D, int DK, int DV, int MODE, bool STEP = false>
 __global__ void __launch_bounds__(warps_for(D) * 32, 1)
 decode_kernel(DecArgs a) {
     constexpr bool FAST = MODE == kModeFast, PACKED = MODE == kModePacked;
-    constexpr bool kStepShape = FAST && D == 128 && DK == 4 && DV == 4;   // decode-step capable
+    static_assert(!STEP || (FAST && D == 128 && DK == 4 && DV == 4), "decode step: 128 / 4 / 4 fast");
+    constexpr int kWarp0 = STEP ? kStepEncodeWarps : 0;   // first warp with a share
     constexpr int kWarps = warps_for(D), kThreads = kWarps * 32;
     constexpr int KSTEPS = D / 16, MT = D / 16;
     constexpr int EK = 2 * DK, EV = 2 * DV;
@@ -936,8 +941,8 @@ decode_kernel(DecArgs a) {
     // ---- fp16 tables replicated per bank group (rows past N are zero)
     if constexpr (FAST) {
         int t0 = 0;   // first thread of the table build
-        if constexpr (kStepShape) {
-            if (a.step) {
+        if constexpr (STEP) {
+            {
                 // ---- decode step: the fp32 codebooks staged, then the new
                 //      tokens encoded into their cache rows by warps 0-3 (one
                 //      token at a time, the codebook split over the 4 warps;
@@ -948,7 +953,7 @@ decode_kernel(DecArgs a) {
                 for (int i = tid; i < nv_f; i += kThreads) stage[nk_f + i] = a.vcbk[i];
                 __syncthreads();
                 pdl_wait();
-                constexpr int kEncWarps = 4;
+                constexpr int kEncWarps = kStepEncodeWarps;
                 static_assert(kThreads - kEncWarps * 32 >= 256, "one table row per builder thread");
                 t0 = kEncWarps * 32;
                 if (warp < kEncWarps) {
@@ -1034,7 +1039,14 @@ decode_kernel(DecArgs a) {
                 c < a.Nv ? pack_h2(stage[nk_f + c * DV + t], stage[nk_f + c * DV + t + 1]) : 0u;
         }
     }
-    __syncthreads();
+    if constexpr (STEP) {
+        // a decode step: the table builders (the warps with shares) meet; the
+        // encoding warps go on to the grid sync
+        if (warp >= kStepEncodeWarps)
+            asm volatile("bar.sync 2, %0;\n" ::"r"((kWarps - kStepEncodeWarps) * 32) : "memory");
+    } else {
+        __syncthreads();
+    }
     // codes (and everything else below) may come from the preceding kernel:
     // wait for it to finish (a no-op unless launched as a dependent)
     pdl_wait();
@@ -1049,7 +1061,9 @@ decode_kernel(DecArgs a) {
 
     // warps past the plan's last one have no share (they still reach the
     // grid syncs of a decode step)
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t gw = warp >= kWarp0
+                           ? (int64_t)blockIdx.x * (kWarps - kWarp0) + (warp - kWarp0)
+                           : (int64_t)a.nw;   // an encoding warp of a decode step: no share
     int64_t t = gw < a.nw ? share_start(gw, a.share, a.total) : 0;
     const int64_t t_end = gw < a.nw ? share_start(gw + 1, a.share, a.total) : 0;
     int slot = 0;
@@ -1106,16 +1120,67 @@ decode_kernel(DecArgs a) {
         // in a decode step, a copy that reads the new rows [new_row0, ..)
         // waits until they are written (the rest of the fill after the sync)
         for (int k = 0; k < kStages; ++k) {
-            if (kStepShape && a.step && pvalid && pj + kStepKeys > a.new_row0) break;
+            if (STEP && pvalid && pj + kStepKeys > a.new_row0) break;
             issue();
         }
     }
+    // ---- transformed queries of a segment's unit's columns into the warp's
+    //      scratch: q~ = Hn (q (.) s_g^-1) (base-2 softmax scale folded in),
+    //      and each column's visible key range
+    auto build_qt = [&](const SegInfo &q) {
+        __syncwarp();
+        for (int col = 0; col < kCols; ++col) {
+            const int cg = q.cblk * kCols + col;
+            if (cg < n_cols_total) {
+                const int i = cg / a.G, gam = cg % a.G;
+                const int hq = q.g * a.G + gam;
+                const __half *qp = a.q + (((int64_t)q.b * a.H_q + hq) * a.S_q + i) * D;
+                const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)q.g * D : a.smooth;
+                // lane holds dims [E lane, E lane + E); FWHT by butterflies in
+                // registers and xor-shuffles
+                constexpr int E = D / 32;
+                float f[E];
+                load_halves<E>(qp + lane * E, f);
+                if (a.smooth_mode != 0) {
+                    float sv[E];
+                    load_floats<E>(sp + lane * E, sv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) f[e] = f[e] / sv[e];
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) f[e] *= a.qscale;
+                reg_fwht<E>(f, lane);
+                store_halves<E>(ws.qt[col] + lane * E, f);
+                if (lane == 0) {
+                    const int L = q.kv_len;
+                    const int q_abs = L - a.S_q + i;
+                    int hi = a.causal ? q_abs : L - 1;
+                    if (hi > L - 1) hi = L - 1;
+                    int lo = a.window > 0 ? q_abs - a.window + 1 : 0;
+                    if (lo < 0) lo = 0;
+                    ws.lo[col] = lo;
+                    ws.hi[col] = hi;
+                }
+            } else {
+                for (int e = lane; e < D; e += 32) ws.qt[col][e] = __float2half_rn(0.f);
+                if (lane == 0) { ws.lo[col] = 1; ws.hi[col] = 0; }   // empty
+            }
+            __syncwarp();
+        }
+    };
+    bool qt_ready = false;   // the first segment's q~ already built
     // ---- decode step: every new token's codes are in the cache (encoded
     //      with the table build above), then a grid sync (the attention below
-    //      reads them through the bulk copies, which need the proxy fence)
-    if constexpr (kStepShape) {
-        if (a.step) {
-            __threadfence();
+    //      reads them through the bulk copies, which need the proxy fence);
+    //      the first segment's queries are transformed before it
+    if constexpr (STEP) {
+        {
+            if (t < t_end) {
+                build_qt(segment_at(a, t, t_end));
+                qt_ready = true;
+            }
+            // (the grid sync orders every thread's writes before it, the code
+            // rows included)
             cooperative_groups::this_grid().sync();
             asm volatile("fence.proxy.async.global;\n" ::: "memory");
             if constexpr (RING) {
@@ -1129,7 +1194,7 @@ decode_kernel(DecArgs a) {
     while (t < t_end) {
         const SegInfo sg = segment_at(a, t, t_end);
         const int64_t seg_end = sg.seg_end, bg = sg.bg;
-        const int cblk = sg.cblk, g = sg.g, b = sg.b, kv_len = sg.kv_len;
+        const int cblk = sg.cblk;
         const int j_first = sg.j_first, j_last = sg.j_last;
         // the segment's first code tiles go to L2 while the queries are prepared
         const uint8_t *kg = a.kc + bg * a.stride * ktb;
@@ -1148,46 +1213,10 @@ decode_kernel(DecArgs a) {
         };
         if constexpr (!RING) prefetch(j_first, kPrefetchTiles * kTile);
 
-        // ---- transformed queries of the unit's columns: q~ = Hn (q (.) s_g^-1)
-        __syncwarp();
-        for (int col = 0; col < kCols; ++col) {
-            const int cg = cblk * kCols + col;
-            if (cg < n_cols_total) {
-                const int i = cg / a.G, gam = cg % a.G;
-                const int hq = g * a.G + gam;
-                const __half *qp = a.q + (((int64_t)b * a.H_q + hq) * a.S_q + i) * D;
-                const float *sp = a.smooth_mode == 2 ? a.smooth + (size_t)g * D : a.smooth;
-                // lane holds dims [E lane, E lane + E); FWHT by butterflies in
-                // registers and xor-shuffles
-                constexpr int E = D / 32;
-                float f[E];
-                load_halves<E>(qp + lane * E, f);
-                if (a.smooth_mode != 0) {
-                    float sv[E];
-                    load_floats<E>(sp + lane * E, sv);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) f[e] = f[e] / sv[e];
-                }
-#pragma unroll
-                for (int e = 0; e < E; ++e) f[e] *= a.qscale;
-                reg_fwht<E>(f, lane);
-                store_halves<E>(ws.qt[col] + lane * E, f);
-                if (lane == 0) {
-                    const int L = kv_len;
-                    const int q_abs = L - a.S_q + i;
-                    int hi = a.causal ? q_abs : L - 1;
-                    if (hi > L - 1) hi = L - 1;
-                    int lo = a.window > 0 ? q_abs - a.window + 1 : 0;
-                    if (lo < 0) lo = 0;
-                    ws.lo[col] = lo;
-                    ws.hi[col] = hi;
-                }
-            } else {
-                for (int e = lane; e < D; e += 32) ws.qt[col][e] = __float2half_rn(0.f);
-                if (lane == 0) { ws.lo[col] = 1; ws.hi[col] = 0; }   // empty
-            }
-            __syncwarp();
-        }
+        // ---- transformed queries of the unit's columns (for a decode step's
+        //      first segment: built before the grid sync)
+        if (qt_ready) qt_ready = false;
+        else build_qt(sg);
         UnitState<D> us;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -1308,10 +1337,9 @@ decode_kernel(DecArgs a) {
     }
     // ---- decode step: every record written, then the merge of the splits
     //      (the codebook table region is free now)
-    if constexpr (kStepShape) {
-        if (a.step) {
-            __threadfence();
-            cooperative_groups::this_grid().sync();
+    if constexpr (STEP) {
+        {
+            cooperative_groups::this_grid().sync();   // orders the records before it
             merge_items<D, kWarps>(a, reinterpret_cast<float *>(ktab), warp, lane);
         }
     }
@@ -1528,6 +1556,14 @@ cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t
         else
             return cudaErrorInvalidValue;
     }
+    if (da.step) {
+        if constexpr (D == 128 && DK == 4 && DV == 4) {
+            if (tb.mode != kModeFast) return cudaErrorInvalidValue;
+            kern = decode_kernel<D, DK, DV, kModeFast, true>;
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tb.bytes);
     if (err != cudaSuccess) return err;
@@ -1635,7 +1671,7 @@ int decode_step_supported(const vq_attend_args &a) {
 // Work split: the (unit, key tile) space, units = (b, kv head, column
 // block), is cut into equal contiguous shares, one per warp of a persistent
 // grid of one CTA per SM (fewer when the problem is small).
-AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
+AttendPlan plan_decode(const vq_attend_args &a, int num_sms, int reserved_warps) {
     AttendPlan p{};
     p.cols = kCols;
     const int ncols = (a.H_q / a.H_kv) * a.S_q;
@@ -1646,7 +1682,7 @@ AttendPlan plan_decode(const vq_attend_args &a, int num_sms) {
     p.tiles = T;
     const int64_t units = (int64_t)a.B * a.H_kv * p.n_colblk;
     p.total = units * T;
-    const int kWarps = warps_for(a.D);
+    const int kWarps = warps_for(a.D) - reserved_warps;   // warps with a share per CTA
     int64_t nw = (int64_t)num_sms * kWarps;
     const int64_t by_size = (p.total + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
     if (nw > by_size) nw = by_size;

@@ -476,7 +476,10 @@ struct AttendPlan {
     int slots;          // partial records per warp
     size_t ws_bytes;    // partial records
 };
-AttendPlan plan_decode(const vq_attend_args &a, int num_sms);
+// reserved_warps: warps of every CTA that take no share (a decode step's
+// encoding warps, kStepEncodeWarps)
+constexpr int kStepEncodeWarps = 4;
+AttendPlan plan_decode(const vq_attend_args &a, int num_sms, int reserved_warps = 0);
 // The same plan with at most max_ws_bytes of partial results (fewer key
 // splits); n_split == 0 when even one split does not fit.
 AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,

@@ -249,10 +249,15 @@ int vq_decode_step(const vq_attend_args *in, const void *k_new_f16, const void *
     int sms = 0;
     rc = current_sms(&sms);
     if (rc != VQ_OK) return rc;
-    const vqkv::AttendPlan plan = vqkv::plan_decode(*a, sms);
+    const bool one_launch = vqkv::decode_step_supported(*a) == VQ_OK;
+    // the single launch keeps kStepEncodeWarps warps of every CTA for the
+    // encode: fewer warps with shares, so its records fit in what
+    // vq_attend_workspace_bytes reports
+    const vqkv::AttendPlan plan =
+        vqkv::plan_decode(*a, sms, one_launch ? vqkv::kStepEncodeWarps : 0);
     if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return VQ_ERR_WORKSPACE;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (vqkv::decode_step_supported(*a) == VQ_OK)
+    if (one_launch)
         return vqkv::launch_decode(*a, plan, st, k_new_f16, v_new_f16) == cudaSuccess ? VQ_OK
                                                                                  : VQ_ERR_CUDA;
     // other shapes: the appends and the attention as separate launches
