@@ -93,6 +93,19 @@ def pack_rows(codes, bits, torch):
     return (out - ((out >> 31) << 32)).to(torch.int32).contiguous()
 
 
+def unpack_rows(rows, n, bits):
+    """Inverse of pack_rows on the host: int32 rows [..., words] -> codes
+    [..., n] (int64)."""
+    w = rows.reshape(-1, rows.shape[-1]).view(np.uint32).astype(np.uint64)
+    w = np.concatenate([w, np.zeros((w.shape[0], 1), np.uint64)], axis=1)
+    out = np.zeros((w.shape[0], n), np.int64)
+    for m in range(n):
+        i, sh = divmod(m * bits, 32)
+        v = (w[:, i] | (w[:, i + 1] << np.uint64(32))) >> np.uint64(sh)
+        out[:, m] = (v & np.uint64((1 << bits) - 1)).astype(np.int64)
+    return out.reshape(rows.shape[:-1] + (n,))
+
+
 def algorithmic(name, spec, lens=None):
     """(dominant kernel, bound, work per launch, unit) -- the per-unit
     figures are stated with the design notes."""
@@ -448,6 +461,9 @@ def run_gpu(args, name, rank, world):
         gpu_out = {}
         if name in ("decode-1seq", "bulk-encode"):
             gpu_out["k_codes"] = r.d["k_codes"].cpu().numpy()
+        elif name == "bulk-encode-packed":
+            gpu_out["k_codes"] = unpack_rows(r.d["k_codes"].cpu().numpy(), spec.n_k,
+                                             _bits(spec.k_N))
         elif not name.startswith("bulk-encode"):
             gpu_out["out"] = r.d["out"].float().cpu().numpy()
         cb = cpu_baseline(name, spec, inp, budget_s=args.cpu_budget, gpu=gpu_out)

@@ -36,6 +36,15 @@ def test_pack_rows_matches_bit_by_bit_packing():
             assert got[idx].tolist() == _row_bit_by_bit(codes[idx], bits), (n, N, idx)
 
 
+def test_unpack_rows_inverts_pack_rows():
+    rng = np.random.default_rng(1)
+    for n, N in [(16, 1024), (32, 1000), (7, 65536), (5, 3)]:
+        bits = bench._bits(N)
+        codes = rng.integers(0, N, size=(4, 3, n))
+        rows = bench.pack_rows(torch.from_numpy(codes), bits, torch).numpy()
+        assert np.array_equal(bench.unpack_rows(rows, n, bits), codes)
+
+
 def test_bits_per_code():
     assert [bench._bits(n) for n in (2, 3, 4, 256, 257, 1000, 1024, 1025)] == \
         [1, 2, 2, 8, 9, 10, 10, 11]
