@@ -538,10 +538,15 @@ def cpu_baseline(name, spec, inp, budget_s=10.0, gpu=None):
         return time.perf_counter() - t0, (b, g, rows), out
 
     def attend_model(pair):
+        """(per-head cost, per-row cost, seconds spent, rows, their outputs):
+        one row and 1 + kExtra rows of the same head, the difference over
+        kExtra rows giving the per-row cost (enough rows that it stands
+        above the run-to-run noise of the per-head part)."""
+        kExtra = 16
         t1 = attend_sample(pair, 1)[0]
-        t5, where, out = attend_sample(pair, 5)
-        per_row = max((t5 - t1) / 4, 0.0)
-        return max(t1 - per_row, 0.0), per_row, t1 + t5, where, out
+        tn, where, out = attend_sample(pair, 1 + kExtra)
+        per_row = max((tn - t1) / kExtra, 0.0)
+        return max(t1 - per_row, 0.0), per_row, t1 + tn, where, out
 
     def attend_parity(where, out):
         if gpu is None or "out" not in gpu:
@@ -569,7 +574,7 @@ def cpu_baseline(name, spec, inp, budget_s=10.0, gpu=None):
             wall = _concurrent_wall(attend_model, list(range(cores)))
             full1 += n_bg * ph + n_rows * pr
             fullN += (n_bg * ph + n_rows * pr) * wall / (cores * tt)
-            sample += (f"; oracle attention of 1 and 5 rows of one kv head over "
+            sample += (f"; oracle attention of 1 and 17 rows of one kv head over "
                        f"{spec.S_kv} keys, scaled to {n_bg} heads and {n_rows} rows")
             value1, valueN = spec.B * spec.S_q / full1, spec.B * spec.S_q / fullN
         else:
@@ -582,7 +587,7 @@ def cpu_baseline(name, spec, inp, budget_s=10.0, gpu=None):
         frac = float(np.mean(inp["kv_lens"])) / spec.S_kv if "kv_lens" in inp else 1.0
         full1 = (n_bg * ph + n_rows * pr) * frac
         fullN = full1 * wall / (cores * tt)
-        sample = (f"oracle attention of 1 and 5 rows of one (batch, kv head) over "
+        sample = (f"oracle attention of 1 and 17 rows of one (batch, kv head) over "
                   f"{spec.S_kv} keys (per thread), scaled to {n_bg} pairs and {n_rows} rows")
         if frac != 1.0:
             sample += f" and by the mean cache length ({frac:.3f} of S_kv)"
