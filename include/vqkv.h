@@ -265,7 +265,7 @@ VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
  * most 256 centroids this is one cooperative launch (encode, grid sync,
  * attention, grid sync, merge of the key splits); other shapes run as the
  * three calls on the same stream.  The workspace is as for
- * vq_decode_attend.
+ * vq_decode_attend (the single launch needs no more than that size).
  * Errors: those of vq_decode_attend and of the encodes; VQ_ERR_SHAPE when
  * S_q > S_kv, VQ_ERR_UNSUPPORTED when kv_lens is given, VQ_ERR_NULL /
  * VQ_ERR_ALIGN for the new tokens, VQ_ERR_CUDA when the launch fails (e.g.
@@ -275,14 +275,16 @@ VQ_API int vq_decode_step(const vq_attend_args *args, const void *k_new_f16,
                           const void *v_new_f16, void *stream);
 
 /*
- * Same operation through the tcgen05 tensor-core path (key/value tiles
- * rebuilt from codes in shared memory, Q~K~^T and PV on the tensor cores,
- * accumulators in tensor memory).  Used when S_q >= 64; smaller S_q, or
- * shapes outside the tensor-core kernel's limits (D != 128, sub_dim != 4,
- * codes wider than one byte), are served by vq_decode_attend with the same
- * arguments.  Each block runs two query heads of a KV group (sharing the
- * rebuilt tiles); with an odd GQA group size H_q / H_kv the last block of a
- * group runs a single head.  Page: "Metal
+ * Same operation through the tcgen05 tensor-core path (code tiles brought
+ * into shared memory by tensor copies, key/value tiles rebuilt from them,
+ * Q~K~^T and PV on the tensor cores, accumulators in tensor memory).  Used
+ * when S_q >= 64; smaller S_q, shapes outside the tensor-core kernel's
+ * limits (D != 128, sub_dim != 4, codes wider than one byte), and code
+ * buffers of 2^31 rows or more (B * H_kv * rows, the tensor copies' row
+ * coordinate), are served by vq_decode_attend with the same arguments.
+ * Each block runs two query heads of a KV group (sharing the rebuilt
+ * tiles); with an odd GQA group size H_q / H_kv the last block of a group
+ * runs a single head.  Page: "Metal
  * Kernels API", section "Fused SDPA", metal_fused_sdpa; the prefill-shaped
  * tile loop follows the companion described under rabitq_prefill_attend.
  * Errors as vq_decode_attend.
