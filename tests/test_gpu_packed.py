@@ -175,3 +175,26 @@ def test_packed_key_path_gqa_window_lengths(S_q, window, Nk):
     ok, err, _ = parity.allclose_report(full.cpu().numpy().astype(np.float64),
                                         oracle.to_f16(ref).astype(np.float64))
     assert ok, f"max |err| {err}"
+
+
+def test_gqa_decode_packed_full_size_whole_groups():
+    """The 10-bit packed-key decode workload at full size (B=32, H_q=32,
+    H_kv=8, S_kv=32768) in the launch the benchmark times: every query head
+    of the first and the last batch, against the oracle over the same codes.
+    The cache is packed here, batch by batch, by this file's own packer."""
+    from _gpu_helpers import oracle_attend_rows_parallel
+    from product_vq_compressed_gb300.workloads import WORKLOADS, make_inputs
+    spec = WORKLOADS["gqa-decode-packed"]
+    inp = make_inputs(spec)
+    kc = inp["k_codes"]
+    bits = bits_for(spec.k_N)
+    kp = np.concatenate([pack(kc[b:b + 1], bits) for b in range(spec.B)])
+    out = vq.decode_attend(dev(inp["q"]), dev(kp), dev(inp["k_codebook"]),
+                           dev(inp["v_codes"]), dev(inp["v_codebook"]), dev(inp["smooth"]),
+                           spec.sm_scale, causal=spec.causal, sliding_window=spec.window)
+    torch.cuda.synchronize()
+    rows = np.array([(b, h, 0) for b in (0, spec.B - 1) for h in range(spec.H_q)])
+    ref = oracle_attend_rows_parallel(inp, spec, rows, kc, inp["v_codes"])
+    got = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    ok, err, excess = parity.allclose_report(got, ref)
+    assert ok, f"max |err| {err}, worst excess {excess}"
