@@ -262,10 +262,15 @@ VQ_API int vq_decode_attend(const vq_attend_args *args, void *stream);
  *              would; then every query attends over rows 0 .. S_kv - 1 as
  *              in vq_decode_attend.  kv_lens must be NULL.
  * With D = 128, 4-dimensional sub-vectors, uint8 codes and codebooks of at
- * most 256 centroids this is one cooperative launch (encode, grid sync,
- * attention, grid sync, merge of the key splits); other shapes run as the
- * three calls on the same stream.  The workspace is as for
- * vq_decode_attend (the single launch needs no more than that size).
+ * most 256 centroids this is one cooperative launch: the encode beside the
+ * attention over the rows before the new ones (a reader of a new row waits,
+ * bounded, for a per-row flag in the workspace that the encode sets), then a
+ * grid sync and the merge of the key splits; other shapes run as the three
+ * calls on the same stream.  The workspace is sized by
+ * vq_attend_workspace_bytes for these args (the single launch keeps its
+ * partial records and flags inside that size); it must not be in use by
+ * another call at the same time.  The launch leaves the flags cleared, so
+ * a workspace can serve consecutive steps and a captured CUDA graph.
  * Errors: those of vq_decode_attend and of the encodes; VQ_ERR_SHAPE when
  * S_q > S_kv, VQ_ERR_UNSUPPORTED when kv_lens is given, VQ_ERR_NULL /
  * VQ_ERR_ALIGN for the new tokens, VQ_ERR_CUDA when the launch fails (e.g.

@@ -30,6 +30,8 @@
 //     skipped by clipping each item's key range.
 //   * Each CTA merges its warps and writes one partial (m, l, o[D]) per
 //     column; the combine kernel merges the splits and writes fp16.
+#include <atomic>
+#include <chrono>
 #include <climits>
 #include <cooperative_groups.h>
 #include <math.h>
@@ -298,11 +300,16 @@ struct DecArgs {
     int slots;         // partial records per warp
     int k_copies, v_copies;
     // one decode step in one cooperative launch (vq_decode_step): encode the
-    // new tokens into cache rows new_row0 .., grid sync, attend, grid sync,
-    // merge the key splits
+    // new tokens into cache rows new_row0 .. beside the attention over the
+    // rows before them, attend over the new rows once their codes are
+    // written, grid sync, merge the key splits
     int step;
     const __half *k_new, *v_new;   // [B, H_kv, S_q, D]
     int new_row0;
+    // per (new token, K / V): step_epoch once its code row is written (in
+    // the workspace; set back to 0 after the final grid sync)
+    unsigned long long *step_flags;
+    unsigned long long step_epoch;   // odd, never 0
     int log2D;
     __half *out;
 };
@@ -707,6 +714,34 @@ __device__ __forceinline__ void process_step(const StepCodes<D, DK, DV> &sc, int
     }
 }
 
+// A decode step's new code rows: written by the encoding warps, announced by
+// a release store of the launch's epoch per (token, K / V); a warp that
+// copies a new row first waits (bounded) for both flags of every new token
+// of its (batch, KV head).  The launch is cooperative, so the encoding CTAs
+// are resident while others wait.
+constexpr uint32_t kFlagWaitLimit = 1u << 22;   // x ~64 ns: ~0.3 s
+__device__ __forceinline__ void flag_release(unsigned long long *f, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(f), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long *f) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+// One lane: false when a flag was not set within the limit.
+__device__ __forceinline__ bool wait_new_rows(const unsigned long long *flags,
+                                              unsigned long long epoch, int64_t bg, int S_q) {
+    for (int i = 0; i < 2 * S_q; ++i) {
+        const unsigned long long *f = flags + 2 * bg * S_q + i;
+        uint32_t it = 0;
+        while (flag_acquire(f) != epoch) {
+            if (++it > kFlagWaitLimit) return false;
+            __nanosleep(64);
+        }
+    }
+    return true;
+}
+
 // Encode of one new token by a group of NW warps, D = 32 E with sub-vectors
 // of E dimensions (lane m owns sub-vector m), into its 32-byte uint8 code row
 // (cb: the fp32 codebook, staged in shared memory by the caller): the same
@@ -886,9 +921,9 @@ __device__ void merge_items(const DecArgs &a, float *sm, int warp, int lane) {
 }
 
 // STEP: the single-launch decode step (vq_decode_step): the new tokens'
-// encode, the attention and the merge of the key splits, with grid syncs
-// between them (a cooperative launch); only the 128 / 4 / 4 fast
-// instantiation has it.
+// encode beside the attention (a copy of new rows waits for their flags),
+// then a grid sync and the merge of the key splits (a cooperative launch);
+// only the 128 / 4 / 4 fast instantiation has it.
 template <int D, int DK, int DV, int MODE, bool STEP = false>
 __global__ void __launch_bounds__(warps_for(D) * 32, 1)
 decode_kernel(DecArgs a) {
@@ -978,6 +1013,11 @@ decode_kernel(DecArgs a) {
                         encode_token_group<4, kEncWarps>(
                             x, smr, !is_v, is_v ? stage + a.Nk * DK : stage, is_v ? a.Nv : a.Nk,
                             dst, a.log2D, lane, warp, xch, kXStride, 1);
+                        if (warp == 0) {   // the group's first warp wrote the row
+                            __threadfence();
+                            __syncwarp();
+                            if (lane == 0) flag_release(a.step_flags + task, a.step_epoch);
+                        }
                     }
                 }
             }
@@ -986,9 +1026,12 @@ decode_kernel(DecArgs a) {
         // row half holds 16 / EK (16 / EV) copies of its centroid.  A thread
         // owns whole rows: both centroid loads are in flight together, then
         // the 16 stores.
+        // (a decode step reads the fp32 codebooks it has staged)
+        const float *kcb_src = STEP ? stage : a.kcbk;
+        const float *vcb_src = STEP ? stage + a.Nk * DK : a.vcbk;
         for (int c = tid - t0; c >= 0 && c < 256; c += kThreads - t0) {
-            const uint4 wk = c < a.Nk ? replica_chunk<DK>(a.kcbk + c * DK) : make_uint4(0u, 0u, 0u, 0u);
-            const uint4 wv = c < a.Nv ? replica_chunk<DV>(a.vcbk + c * DV) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 wk = c < a.Nk ? replica_chunk<DK>(kcb_src + c * DK) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 wv = c < a.Nv ? replica_chunk<DV>(vcb_src + c * DV) : make_uint4(0u, 0u, 0u, 0u);
             uint4 *row = reinterpret_cast<uint4 *>(ktab + c * kFastRow);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -1060,7 +1103,7 @@ decode_kernel(DecArgs a) {
     WarpScratch<D> &ws = scratch[warp];
 
     // warps past the plan's last one have no share (they still reach the
-    // grid syncs of a decode step)
+    // grid sync of a decode step)
     const int64_t gw = warp >= kWarp0
                            ? (int64_t)blockIdx.x * (kWarps - kWarp0) + (warp - kWarp0)
                            : (int64_t)a.nw;   // an encoding warp of a decode step: no share
@@ -1085,8 +1128,26 @@ decode_kernel(DecArgs a) {
         }
     };
     // copy the next step's K and V code rows into stage issued % kStages
+    // (in a decode step, rows from new_row0 on once they are written)
+    int64_t new_ok_bg = -1;   // (b, kv head) whose new rows this warp has seen written
     auto issue = [&]() {
         if (!pvalid) return;
+        if constexpr (STEP) {
+            if (pj + kStepKeys > a.new_row0 && ps.bg != new_ok_bg) {
+                bool ok = true;
+                if (lane == 0) ok = wait_new_rows(a.step_flags, a.step_epoch, ps.bg, a.S_q);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {   // the records of this warp become NaN
+                    ring_ok = false;
+                    pvalid = false;
+                    return;
+                }
+                new_ok_bg = ps.bg;
+                // the rows were written through the generic proxy; the copies
+                // read them through the async proxy
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            }
+        }
         const int sidx = issued % kStages;
         const uint32_t bar = wbar + (uint32_t)(sidx * 8);
         const uint32_t st = wring + (uint32_t)(sidx * RC::STAGE);
@@ -1169,23 +1230,16 @@ decode_kernel(DecArgs a) {
         }
     };
     bool qt_ready = false;   // the first segment's q~ already built
-    // ---- decode step: every new token's codes are in the cache (encoded
-    //      with the table build above), then a grid sync (the attention below
-    //      reads them through the bulk copies, which need the proxy fence);
-    //      the first segment's queries are transformed before it
+    // ---- decode step: the first segment's queries are transformed, then the
+    //      rest of the ring is filled; a copy of new rows waits there for
+    //      their flags (set by the encoding warps, which run beside this)
     if constexpr (STEP) {
-        {
-            if (t < t_end) {
-                build_qt(segment_at(a, t, t_end));
-                qt_ready = true;
-            }
-            // (the grid sync orders every thread's writes before it, the code
-            // rows included)
-            cooperative_groups::this_grid().sync();
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
-            if constexpr (RING) {
-                while (pvalid && issued < kStages) issue();   // nothing consumed yet
-            }
+        if (t < t_end) {
+            build_qt(segment_at(a, t, t_end));
+            qt_ready = true;
+        }
+        if constexpr (RING) {
+            while (pvalid && issued < kStages) issue();   // nothing consumed yet
         }
     }
 
@@ -1340,6 +1394,10 @@ decode_kernel(DecArgs a) {
     if constexpr (STEP) {
         {
             cooperative_groups::this_grid().sync();   // orders the records before it
+            // every wait for new rows is over: their flags back to 0 for
+            // the next launch on this workspace (a replayed graph included)
+            if (blockIdx.x == 0)
+                for (int i = tid; i < 2 * a.B * a.H_kv * a.S_q; i += kThreads) a.step_flags[i] = 0ull;
             merge_items<D, kWarps>(a, reinterpret_cast<float *>(ktab), warp, lane);
         }
     }
@@ -1568,9 +1626,9 @@ cudaError_t launch_t(const DecArgs &da, const Tables &tb, int grid, cudaStream_t
                                            (int)tb.bytes);
     if (err != cudaSuccess) return err;
     if (da.step) {
-        // a decode step: cooperative launch (its blocks meet at grid syncs;
-        // the launch fails rather than starting if they cannot all be
-        // resident at once)
+        // a decode step: cooperative launch (its blocks meet at a grid sync
+        // and wait on one another's flags; the launch fails rather than
+        // starting if they cannot all be resident at once)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(warps_for(D) * 32);
@@ -1666,6 +1724,13 @@ int decode_step_supported(const vq_attend_args &a) {
     if (a.kv_lens) return VQ_ERR_UNSUPPORTED;
     if (choose_tables(a).mode != kModeFast) return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
+}
+
+// A decode step's flags (one 8-byte word per new token and K / V) follow the
+// partial records in the workspace.
+size_t step_flags_offset(const AttendPlan &plan) { return (plan.ws_bytes + 15) & ~(size_t)15; }
+size_t step_flags_bytes(const vq_attend_args &a) {
+    return 2 * (size_t)a.B * a.H_kv * a.S_q * sizeof(unsigned long long);
 }
 
 // Work split: the (unit, key tile) space, units = (b, kv head, column
@@ -1766,6 +1831,16 @@ cudaError_t launch_decode(const vq_attend_args &a, const AttendPlan &plan,
     da.k_new = reinterpret_cast<const __half *>(k_new);
     da.v_new = reinterpret_cast<const __half *>(v_new);
     da.new_row0 = a.S_kv - a.S_q;
+    if (da.step) {
+        // the new rows' flags after the records; a fresh odd epoch per launch
+        // (flags left by an earlier launch are 0, and memory never written
+        // by one matches an epoch only by a 2^-64 chance)
+        static std::atomic<unsigned long long> epoch{
+            (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 2ull + 1ull};
+        da.step_flags = reinterpret_cast<unsigned long long *>(
+            reinterpret_cast<unsigned char *>(a.workspace) + step_flags_offset(plan));
+        da.step_epoch = epoch.fetch_add(2ull);
+    }
     int l2d = 0;
     while ((1 << l2d) < a.D) ++l2d;
     da.log2D = l2d;

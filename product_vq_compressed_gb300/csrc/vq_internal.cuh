@@ -480,6 +480,10 @@ struct AttendPlan {
 // encoding warps, kStepEncodeWarps)
 constexpr int kStepEncodeWarps = 4;
 AttendPlan plan_decode(const vq_attend_args &a, int num_sms, int reserved_warps = 0);
+// A decode step's flags for its new rows: their offset in the workspace
+// (after the plan's partial records) and size.
+size_t step_flags_offset(const AttendPlan &plan);
+size_t step_flags_bytes(const vq_attend_args &a);
 // The same plan with at most max_ws_bytes of partial results (fewer key
 // splits); n_split == 0 when even one split does not fit.
 AttendPlan plan_decode_capped(const vq_attend_args &a, int num_sms,

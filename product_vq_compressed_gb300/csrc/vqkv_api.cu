@@ -225,7 +225,9 @@ size_t vq_attend_workspace_bytes(const vq_attend_args *args) {
         return 0;
     int sms = 0;
     if (current_sms(&sms) != VQ_OK) return 0;
-    return vqkv::plan_decode(*a, sms).ws_bytes;
+    // (+ the flags of a single-launch decode step, whose own plan has fewer
+    // warps with records)
+    return vqkv::step_flags_offset(vqkv::plan_decode(*a, sms)) + vqkv::step_flags_bytes(*a);
 }
 
 int vq_decode_attend(const vq_attend_args *args, void *stream) {
@@ -255,7 +257,9 @@ int vq_decode_step(const vq_attend_args *in, const void *k_new_f16, const void *
     // vq_attend_workspace_bytes reports
     const vqkv::AttendPlan plan =
         vqkv::plan_decode(*a, sms, one_launch ? vqkv::kStepEncodeWarps : 0);
-    if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return VQ_ERR_WORKSPACE;
+    const size_t need = one_launch ? vqkv::step_flags_offset(plan) + vqkv::step_flags_bytes(*a)
+                                   : plan.ws_bytes;
+    if (!a->workspace || a->workspace_bytes < need) return VQ_ERR_WORKSPACE;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (one_launch)
         return vqkv::launch_decode(*a, plan, st, k_new_f16, v_new_f16) == cudaSuccess ? VQ_OK
