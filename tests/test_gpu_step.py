@@ -93,6 +93,36 @@ def test_decode_step_matches_oracle_and_separate_calls(B, H_q, H_kv, S_kv, S_q, 
         assert ok, f"step vs oracle: max |err| {err}"
 
 
+def test_decode_step_on_a_workspace_of_stale_bytes():
+    """The single launch's new rows are announced through flags in the
+    workspace; a workspace that holds arbitrary bytes (here random ones,
+    as left by other calls) and a second step on the same workspace give
+    the same result as the separate calls."""
+    x = _case(31, 2, 8, 2, 1500, 1, 1600)
+    d, D, S_kv = x["d"], x["D"], x["S_kv"]
+    kcb, vcb, smooth = dev(x["kcb"]), dev(x["vcb"]), dev(x["smooth"])
+    kbuf, vbuf = dev(x["kc"]), dev(x["vc"])
+    q = dev(x["q"])
+    out = torch.empty_like(q)
+    args = vq.make_attend_args(q, kbuf, kcb, vbuf, vcb, smooth, 1 / np.sqrt(D), True, 0, out,
+                               s_kv=S_kv)
+    n = max(vq.attend_workspace_bytes(args), 16)
+    ws = torch.from_numpy(np.random.default_rng(3).integers(0, 256, n, dtype=np.uint8)).to(DEV)
+    kb2, vb2 = dev(x["kc"]), dev(x["vc"])
+    for step in range(2):
+        k_new = x["k_new"] if step == 0 else x["k_new"][..., ::-1].copy()
+        v_new = x["v_new"] if step == 0 else x["v_new"][..., ::-1].copy()
+        vq.decode_step(q, dev(k_new), dev(v_new), kbuf, kcb, vbuf, vcb, smooth, 1 / np.sqrt(D),
+                       out=out, workspace=ws, s_kv=S_kv)
+        vq.encode_keys_into(dev(k_new), kcb, d, smooth, kb2, S_kv - 1)
+        vq.encode_values_into(dev(v_new), vcb, d, vb2, S_kv - 1)
+        ref = vq.decode_attend(q, kb2, kcb, vb2, vcb, smooth, 1 / np.sqrt(D), s_kv=S_kv)
+        torch.cuda.synchronize()
+        assert torch.equal(kbuf, kb2) and torch.equal(vbuf, vb2), step
+        ok, err, _ = parity.allclose_report(out.float().cpu().numpy(), ref.float().cpu().numpy())
+        assert ok, f"step {step}: max |err| {err}"
+
+
 def test_decode_step_other_shapes_run_as_separate_calls():
     """D = 64 has no single-launch path: the same result through the three
     calls on the stream."""
