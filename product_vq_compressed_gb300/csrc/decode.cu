@@ -1268,7 +1268,7 @@ decode_kernel(DecArgs a) {
         if constexpr (!RING) prefetch(j_first, kPrefetchTiles * kTile);
 
         // ---- transformed queries of the unit's columns (for a decode step's
-        //      first segment: built before the grid sync)
+        //      first segment: built before the ring is filled)
         if (qt_ready) qt_ready = false;
         else build_qt(sg);
         UnitState<D> us;
