@@ -93,6 +93,36 @@ def test_decode_step_matches_oracle_and_separate_calls(B, H_q, H_kv, S_kv, S_q, 
         assert ok, f"step vs oracle: max |err| {err}"
 
 
+@pytest.mark.parametrize("S_q,window", [(1, 500), (2, 1), (3, 130)])
+def test_decode_step_with_a_sliding_window(S_q, window):
+    """A sliding window (the new rows are always inside it; a window of 1
+    leaves each query only its own row): the step against the separate calls
+    and against the oracle over the updated cache."""
+    B, H_q, H_kv, S_kv, cap = 2, 8, 2, 3000, 3010
+    x = _case(S_q * 100 + window, B, H_q, H_kv, S_kv, S_q, cap)
+    d, D = x["d"], x["D"]
+    kcb, vcb, smooth = dev(x["kcb"]), dev(x["vcb"]), dev(x["smooth"])
+    kbuf, vbuf = dev(x["kc"]), dev(x["vc"])
+    out = vq.decode_step(dev(x["q"]), dev(x["k_new"]), dev(x["v_new"]), kbuf, kcb, vbuf, vcb,
+                         smooth, 1 / np.sqrt(D), sliding_window=window, s_kv=S_kv)
+    kb2, vb2 = dev(x["kc"]), dev(x["vc"])
+    vq.encode_keys_into(dev(x["k_new"]), kcb, d, smooth, kb2, S_kv - S_q)
+    vq.encode_values_into(dev(x["v_new"]), vcb, d, vb2, S_kv - S_q)
+    ref2 = vq.decode_attend(dev(x["q"]), kb2, kcb, vb2, vcb, smooth, 1 / np.sqrt(D),
+                            sliding_window=window, s_kv=S_kv)
+    torch.cuda.synchronize()
+    assert torch.equal(kbuf, kb2) and torch.equal(vbuf, vb2)
+    got = out.float().cpu().numpy()
+    ok, err, _ = parity.allclose_report(got, ref2.float().cpu().numpy())
+    assert ok, f"step vs separate calls: max |err| {err}"
+    kb, vb = kbuf.cpu().numpy(), vbuf.cpu().numpy()
+    ref = oracle.attend(x["q"], kb[:, :, :S_kv].astype(np.int64), x["kcb"],
+                        vb[:, :, :S_kv].astype(np.int64), x["vcb"], x["smooth"], 1 / np.sqrt(D),
+                        causal=True, sliding_window=window)
+    ok, err, _ = parity.allclose_report(got, oracle.to_f16(ref).astype(np.float64))
+    assert ok, f"step vs oracle: max |err| {err}"
+
+
 def test_decode_step_on_a_workspace_of_stale_bytes():
     """The single launch's new rows are announced through flags in the
     workspace; a workspace that holds arbitrary bytes (here random ones,
