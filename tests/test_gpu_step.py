@@ -123,6 +123,37 @@ def test_decode_step_with_a_sliding_window(S_q, window):
     assert ok, f"step vs oracle: max |err| {err}"
 
 
+@pytest.mark.parametrize("smooth_mode", [0, 1])
+def test_decode_step_smooth_layouts(smooth_mode):
+    """No smooth, and one smooth vector [D] shared by the heads: the new
+    keys' codes against the oracle's (near ties only), the caches against
+    the separate calls, the output against the oracle."""
+    B, H_q, H_kv, S_kv, S_q, cap = 1, 8, 4, 900, 1, 960
+    x = _case(50 + smooth_mode, B, H_q, H_kv, S_kv, S_q, cap)
+    d, D = x["d"], x["D"]
+    sm = None if smooth_mode == 0 else x["smooth"][0].copy()
+    kcb, vcb = dev(x["kcb"]), dev(x["vcb"])
+    smd = None if sm is None else dev(sm)
+    kbuf, vbuf = dev(x["kc"]), dev(x["vc"])
+    out = vq.decode_step(dev(x["q"]), dev(x["k_new"]), dev(x["v_new"]), kbuf, kcb, vbuf, vcb,
+                         smd, 1 / np.sqrt(D), s_kv=S_kv)
+    kb2, vb2 = dev(x["kc"]), dev(x["vc"])
+    vq.encode_keys_into(dev(x["k_new"]), kcb, d, smd, kb2, S_kv - S_q)
+    vq.encode_values_into(dev(x["v_new"]), vcb, d, vb2, S_kv - S_q)
+    torch.cuda.synchronize()
+    assert torch.equal(kbuf, kb2) and torch.equal(vbuf, vb2)
+    kb, vb = kbuf.cpu().numpy(), vbuf.cpu().numpy()
+    new = slice(S_kv - S_q, S_kv)
+    rk = check_encode(x["k_new"], x["kcb"], d, sm, True, kb[:, :, new], None)
+    assert rk["mismatch"] == rk["near_tie"]
+    ref = oracle.attend(x["q"], kb[:, :, :S_kv].astype(np.int64), x["kcb"],
+                        vb[:, :, :S_kv].astype(np.int64), x["vcb"], sm, 1 / np.sqrt(D),
+                        causal=True)
+    ok, err, _ = parity.allclose_report(out.float().cpu().numpy(),
+                                        oracle.to_f16(ref).astype(np.float64))
+    assert ok, f"step vs oracle: max |err| {err}"
+
+
 def test_decode_step_on_a_workspace_of_stale_bytes():
     """The single launch's new rows are announced through flags in the
     workspace; a workspace that holds arbitrary bytes (here random ones,
