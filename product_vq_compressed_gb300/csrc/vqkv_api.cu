@@ -225,9 +225,14 @@ size_t vq_attend_workspace_bytes(const vq_attend_args *args) {
         return 0;
     int sms = 0;
     if (current_sms(&sms) != VQ_OK) return 0;
-    // (+ the flags of a single-launch decode step, whose own plan has fewer
-    // warps with records)
-    return vqkv::step_flags_offset(vqkv::plan_decode(*a, sms)) + vqkv::step_flags_bytes(*a);
+    // the larger of the split-KV plan's records and what a single-launch
+    // decode step keeps there (its own plan's records, which has fewer warps
+    // with longer shares, then the flags of its new rows)
+    const size_t attend = vqkv::plan_decode(*a, sms).ws_bytes;
+    const size_t step =
+        vqkv::step_flags_offset(vqkv::plan_decode(*a, sms, vqkv::kStepEncodeWarps)) +
+        vqkv::step_flags_bytes(*a);
+    return attend > step ? attend : step;
 }
 
 int vq_decode_attend(const vq_attend_args *args, void *stream) {
@@ -253,8 +258,8 @@ int vq_decode_step(const vq_attend_args *in, const void *k_new_f16, const void *
     if (rc != VQ_OK) return rc;
     const bool one_launch = vqkv::decode_step_supported(*a) == VQ_OK;
     // the single launch keeps kStepEncodeWarps warps of every CTA for the
-    // encode: fewer warps with shares, so its records fit in what
-    // vq_attend_workspace_bytes reports
+    // encode (fewer warps with shares); vq_attend_workspace_bytes covers its
+    // records and flags as well as the separate calls' records
     const vqkv::AttendPlan plan =
         vqkv::plan_decode(*a, sms, one_launch ? vqkv::kStepEncodeWarps : 0);
     const size_t need = one_launch ? vqkv::step_flags_offset(plan) + vqkv::step_flags_bytes(*a)
