@@ -225,9 +225,11 @@ typedef struct {
 } vq_attend_args;
 
 /*
- * Scratch bytes vq_decode_attend / vq_prefill_attend need for `args` on the
- * current device (split-KV partial results; 0 if none).  Depends only on the
- * sizes in args and on the device's SM count.  Returns 0 for a NULL args.
+ * Scratch bytes vq_decode_attend / vq_prefill_attend / vq_decode_step need
+ * for `args` on the current device: the split-KV partial results, or for a
+ * single-launch decode step its partial results and the flags of its new
+ * rows, whichever is larger (0 if none).  Depends only on the sizes in args
+ * and on the device's SM count.  Returns 0 for a NULL args.
  */
 VQ_API size_t vq_attend_workspace_bytes(const vq_attend_args *args);
 
