@@ -10,14 +10,20 @@
 // q . K_hat^T with K~ = dequant(codes) in the rotated domain.
 //
 // GB300 design
-//   * Work item = (b, kv head g, column block, key split).  A column is one
-//     (query head of the GQA group, query row) pair; up to 8 columns share
-//     one pass over the codes, so one code fetch serves every query head of
-//     the group.  The kernel is persistent: each CTA stages the codebooks
-//     once and loops over items.
+//   * A unit is (b, kv head g, column block); a column is one (query head of
+//     the GQA group, query row) pair, and up to 8 columns share one pass over
+//     the codes, so one code fetch serves every query head of the group.
+//     The (unit, 16-key tile) space is cut into equal contiguous shares, one
+//     per warp of a persistent grid of one CTA per SM; each warp writes one
+//     partial (m, l, o[D]) per unit it touched and per column, and the
+//     combine kernel merges them and writes fp16.
 //   * Both codebooks live in shared memory as fp16, replicated so that every
-//     copy sits in its own bank group (128 bytes per centroid row, lane l
-//     reads copy l mod C): the random per-lane gathers are conflict-free.
+//     copy sits in its own bank group (lane l reads copy l mod C): the random
+//     per-lane gathers are conflict-free.
+//   * Codes: uint8 code rows of 16-byte multiples arrive through a per-warp
+//     ring of shared-memory stages filled by cp.async.bulk (mbarrier per
+//     stage, bounded waits); 10-bit packed keys of 8 dimensions have their
+//     own mode; other widths are read through the read-only cache.
 //   * Scores and the value sum run on warp-level tensor-core MMA
 //     (m16n8k16, fp16 x fp16 -> fp32) in "swap-AB" form: S^T[16 keys x 8
 //     cols] = K~[16 x D] . Q~^T and O^T[D x 8] += V_hat^T[D x 16] . P^T.
@@ -25,11 +31,12 @@
 //     dimensions are permuted (consistently on both operands) so that one
 //     gather of a whole sub-vector lands in one lane's fragment.  P moves
 //     from accumulator to operand layout with movmatrix.trans.
-//   * Online softmax in base 2 (scale * log2 e applied to the fp32 scores),
-//     per column; masks only on tiles that need them; fully masked tiles are
-//     skipped by clipping each item's key range.
-//   * Each CTA merges its warps and writes one partial (m, l, o[D]) per
-//     column; the combine kernel merges the splits and writes fp16.
+//   * Online softmax in base 2 (scale * log2 e folded into q~), per column,
+//     with a reference maximum that moves only past 2^8; masks only at the
+//     edges of a segment; keys no column can see are clipped away.
+//   * The decode step (STEP instantiation, one cooperative launch): the new
+//     tokens' encode beside the attention, per-row flags for the new code
+//     rows, a grid sync and the merge of the key splits in the kernel.
 #include <atomic>
 #include <chrono>
 #include <climits>
