@@ -56,3 +56,41 @@ def test_packed_decode_algorithmic_bytes():
     _, bound, byts, unit = bench.algorithmic("gqa-decode-packed", s)
     assert bound == "hbm" and unit == "GB/s"
     assert byts == s.B * s.H_kv * s.S_kv * (20 + 32) + 2 * s.B * s.H_q * s.S_q * s.D * 2
+
+
+def test_prefill_flops_count_every_visible_key():
+    """chunked-prefill: 4 D FLOPs (QK^T and PV, a multiply-add each) per query
+    head, query row and visible key.  The visible keys of each row come
+    from the mask's definition (causal: j <= q_abs; window W: j > q_abs - W;
+    q_abs = S_kv - S_q + i), counted row by row."""
+    s = WORKLOADS["chunked-prefill"]
+    _, bound, flops, unit = bench.algorithmic("chunked-prefill", s)
+    assert bound == "tensor" and unit == "TFLOP/s"
+    q_abs = s.S_kv - s.S_q + np.arange(s.S_q)
+    lo = np.maximum(0, q_abs - s.window + 1) if s.window else np.zeros_like(q_abs)
+    hi = q_abs if s.causal else np.full_like(q_abs, s.S_kv - 1)
+    visible = int(np.sum(hi - lo + 1))
+    assert flops == 4 * s.D * s.H_q * s.B * visible
+
+
+def test_decode_bytes_are_the_codes_read_once():
+    """gqa-decode: one uint8 code per sub-vector of every cached key and
+    value, per KV head, plus the fp16 queries read and outputs written;
+    ragged caches count their own lengths."""
+    s = WORKLOADS["gqa-decode"]
+    _, bound, byts, _ = bench.algorithmic("gqa-decode", s)
+    assert bound == "hbm"
+    assert byts == s.B * s.H_kv * s.S_kv * (s.D // s.k_d + s.D // s.v_d) + \
+        2 * s.B * s.H_q * s.S_q * s.D * 2
+    r = WORKLOADS["gqa-decode-ragged"]
+    lens = np.array([r.S_kv // 2, r.S_kv, 5] + [r.S_kv - 1] * (r.B - 3))
+    _, _, rb, _ = bench.algorithmic("gqa-decode-ragged", r, lens)
+    assert rb == r.H_kv * int(lens.sum()) * 64 + 2 * r.B * r.H_q * r.S_q * r.D * 2
+
+
+def test_encode_flops_one_multiply_add_per_dimension_and_candidate():
+    s = WORKLOADS["decode-1seq"]
+    kernel, bound, flops, _ = bench.algorithmic("decode-1seq", s)
+    assert kernel == "encode" and bound == "alu"
+    n_sub = s.B * s.H_kv * s.S_kv * (s.D // s.k_d)
+    assert flops == 2 * s.k_d * s.k_N * n_sub
