@@ -94,3 +94,4 @@ def test_encode_flops_one_multiply_add_per_dimension_and_candidate():
     assert kernel == "encode" and bound == "alu"
     n_sub = s.B * s.H_kv * s.S_kv * (s.D // s.k_d)
     assert flops == 2 * s.k_d * s.k_N * n_sub
+
