@@ -95,3 +95,27 @@ def test_encode_flops_one_multiply_add_per_dimension_and_candidate():
     n_sub = s.B * s.H_kv * s.S_kv * (s.D // s.k_d)
     assert flops == 2 * s.k_d * s.k_N * n_sub
 
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys, on the workload's own metric."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "decode-append", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=300,
+                       cwd=__import__("os").path.dirname(bench.__file__))
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    metric, unit = bench.METRICS["decode-append"][0], bench.METRICS["decode-append"][1]
+    assert d["impl"] == "reference" and d["metric"] == metric and d["unit"] == unit
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 1, 0)
+    assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f64"
+    assert d["config"]["workload"] == "decode-append"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
